@@ -1,0 +1,442 @@
+"""Benchmark of one sparse-embedding training step on GB300.
+
+A step is the whole hot path over one synthetic batch: forward lookup +
+pooling + concatenation, backward dedup, segmented gradient reduction and the
+optimizer update (emb_forward + emb_backward_update through the C ABI).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config dlrm]
+                    [--variant reduction|unique_sort|unique_hash] [--impl ours|reference]
+
+Default workload: the DLRM-style one-hot configuration (26 fp32 tables, rows
+log-uniform in [1e3, 1e7], dim 128, batch 65,536, Zipf(1.05) keys, sum
+pooling, Adagrad).  Tables (~29 GB) and the per-step tensors (out and grad_out,
+872 MB each) are far larger than L2, so no L2 flush is needed between steps.
+
+--impl reference times the CPU oracle (test infrastructure, single-threaded C)
+on a bounded sample of the same workload; it is a reported baseline only.
+Under torchrun every rank runs a full replica (the path has no exchange step);
+rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import ctr_inputs as ci  # noqa: E402
+
+METRIC = "embedding lookups/sec (fwd+bwd+update) on 1 GB300; achieved HBM GB/s vs peak"
+CONFIG_TEXT = {
+    "tiny": "tiny: 4 fp32 tables x 1,000 rows x dim 16, batch 256, hotness U[1,4], uniform keys, sum, SGD",
+    "dlrm": ("DLRM-style one-hot: 26 fp32 tables, rows log-uniform in [1e3,1e7], dim 128, batch 65,536, "
+             "hotness 1, Zipf(1.05) keys, sum pooling, Adagrad lr=0.01 eps=1e-8"),
+    "multihot": ("multi-hot: 100 fp32 tables x 1e6 rows x dim 64, batch 16,384, per-table hotness U[1,100], "
+                 "Zipf(1.2), mean pooling, Adagrad"),
+    "huge": ("single huge table: 1 fp16 table x 2e8 rows x dim 64, fp32 Adagrad state, batch 131,072, "
+             "hotness 20, Zipf(1.1), sum pooling"),
+    "skew": ("skewed dedup stress: 8 fp32 tables dims {16,32,64,128}x2 x 5e6 rows, batch 262,144, hotness 50, "
+             "Zipf(1.5), sum pooling, SGD"),
+}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _wbytes(dtype: str) -> int:
+    return 4 if dtype == "f32" else 2
+
+
+def algorithmic_bytes(w: ci.Workload, batch: ci.Batch, U_per_table: np.ndarray) -> dict:
+    """Bytes each phase must move through HBM at least once (compulsory)."""
+    T, B, nnz = w.num_tables, w.batch, batch.nnz
+    D = w.total_dim
+    rows_bytes = sum(int(U_per_table[t]) * s.dim * _wbytes(s.dtype) for t, s in enumerate(w.tables))
+    state_bytes = sum(int(U_per_table[t]) * s.dim * 4 for t, s in enumerate(w.tables) if s.opt == "adagrad")
+    fwd = 8 * nnz + 8 * (T * B + 1) + 4 * T * B + rows_bytes + 4 * B * D + 8 * nnz   # + gid/bag ids written
+    dedup = 8 * nnz + 8 * nnz                                    # read (id, bag) pairs, write them sorted
+    upd = 4 * B * D + 8 * nnz + 2 * rows_bytes + 2 * state_bytes   # grad once, sorted ids+bags, row/state r+w
+    return {"forward": fwd, "dedup": dedup, "reduce_update": upd, "step": fwd + dedup + upd}
+
+
+def unique_per_table(w: ci.Workload, batch: ci.Batch) -> np.ndarray:
+    B = w.batch
+    U = np.zeros(w.num_tables, dtype=np.int64)
+    for t in range(w.num_tables):
+        k = batch.keys[batch.offsets[t * B]:batch.offsets[(t + 1) * B]]
+        U[t] = np.unique(k).size
+    return U
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.idx = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def oracle_step_timed(w: ci.Workload, batch: ci.Batch, grad: np.ndarray, seed: int) -> float:
+    """Seconds the CPU oracle takes for a1..a5 on `batch` (initial rows prepared untimed)."""
+    import oracle
+    gids, _ = oracle.global_ids(w.tables, w.batch, batch.offsets, batch.keys, batch.table_ids)
+    u, inv, _, _ = oracle.unique(gids, skip_negative=True)
+    rows = oracle.make_row_store(w.tables, u, lambda t, r: ci.init_values(
+        seed, t, r, w.tables[t].dim, w.w_lo, w.w_hi, w.tables[t].dtype))
+    state = oracle.make_row_store(w.tables, u, None, state_init=True)
+    t0 = time.perf_counter()
+    gids, _ = oracle.global_ids(w.tables, w.batch, batch.offsets, batch.keys, batch.table_ids)
+    u, inv, _, _ = oracle.unique(gids, skip_negative=True)
+    oracle.forward(w.tables, w.batch, batch.offsets, inv, rows)
+    G, Gabs = oracle.reduce(w.tables, w.batch, batch.offsets, inv, rows, grad)
+    oracle.update(w.tables, rows, state, G, None)
+    return time.perf_counter() - t0
+
+
+def cpu_sample(w: ci.Workload, sample_batch: int):
+    ws = w.replace(batch=sample_batch)
+    b = ci.make_batch(ws)
+    g = ci.make_grad(ws)
+    return ws, b, g
+
+
+def run_reference(args, w: ci.Workload):
+    ws_, rank, _ = _dist()
+    if rank != 0:
+        return
+    sw, sb, sg = cpu_sample(w, args.cpu_sample_batch)
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle_step_timed(sw, sb, sg, w.seed)
+    secs = [oracle_step_timed(sw, sb, sg, w.seed) for _ in range(args.steps)]
+    per = sum(secs) / len(secs)
+    v = sb.nnz / per
+    sample = "%d of %d samples per table (%d lookups), full step a1..a5, %d timed steps" % (
+        args.cpu_sample_batch, w.batch, sb.nnz, args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "lookups/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3 * w.batch / args.cpu_sample_batch,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": CONFIG_TEXT[args.config], "batch": w.batch,
+                                        "variant": "definition (no dedup variant)"},
+        "cpu_baseline": {"value": v, "unit": "lookups/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="dlrm", choices=sorted(CONFIG_TEXT))
+    ap.add_argument("--variant", default="reduction", choices=["reduction", "unique_sort", "unique_hash"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batches", type=int, default=2, help="distinct seeded batches cycled through")
+    ap.add_argument("--cpu-sample-batch", type=int, default=16384)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch size (small profiling cases)")
+    ap.add_argument("--rows-cap", type=int, default=0, help="cap every table's rows (small profiling cases)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    w = ci.workload(args.config)
+    if args.batch:
+        w = w.replace(batch=args.batch)
+    if args.rows_cap:
+        w = w.replace(tables=tuple(ci.TableSpec(min(t.rows, args.rows_cap), t.dim, t.dtype, t.pooling, t.opt, t.lr,
+                                                t.eps, t.init_acc) for t in w.tables))
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    if rank == 0 or ws == 1:
+        __graft_entry__.build()
+    if ws > 1:
+        dist.barrier(device_ids=[local])
+    from dlrm_sparse_embedding_gb300 import EMB_OK, EmbeddingLayer
+
+    # inputs: a few seeded batches of the same workload, one grad_out
+    batches = [ci.make_batch(w, seed=w.seed + i) for i in range(args.batches)]
+    grad = ci.make_grad(w)
+    max_nnz = max(b.nnz for b in batches)
+    U_t = unique_per_table(w, batches[0])
+    bytes_ = algorithmic_bytes(w, batches[0], U_t)
+
+    dkeys = [torch.from_numpy(b.keys).to(dev) for b in batches]
+    doffs = [torch.from_numpy(b.offsets).to(dev) for b in batches]
+    dtids = [torch.from_numpy(b.table_ids).to(dev) for b in batches]
+    dgrad = torch.from_numpy(grad).to(dev)
+    out = torch.empty((w.batch, w.total_dim), dtype=torch.float32, device=dev)
+
+    layer = EmbeddingLayer(w.tables, w.batch, max_nnz)
+    layer.init_uniform(w.seed, w.w_lo, w.w_hi)
+
+    def step(i):
+        k = i % args.batches
+        layer.forward(dkeys[k], doffs[k], dtids[k], w.batch, out)
+        layer.backward_update(dgrad, args.variant)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    status = layer.sync_status()
+    if status != EMB_OK:
+        raise SystemExit("device status %d after warm-up" % status)
+
+    # ---- device-resident timed region ----
+    layer.set_timing(True)
+    layer.phase_times(reset=True)
+    layer.launch_count(reset=True)
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    if ws > 1:
+        dist.barrier(device_ids=[local])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier(device_ids=[local])
+    clk = clocks.stop() if rank == 0 else None
+    ms = e0.elapsed_time(e1) / args.steps
+    phases, nsteps = layer.phase_times(reset=True)
+    launches = layer.launch_count(reset=True)
+    layer.set_timing(False)
+    status = layer.sync_status()
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end: host buffers, copies inside the timed region ----
+    # Every step copies its inputs (keys, offsets, table ids, grad_out) from
+    # pinned host memory and reads the pooled output back.  The copies run on
+    # their own streams, double-buffered, so step i's compute overlaps the
+    # upload of step i+1 and the download of step i-1.
+    e2e = None
+    if not args.no_e2e:
+        hk = [torch.from_numpy(b.keys).pin_memory() for b in batches]
+        ho = [torch.from_numpy(b.offsets).pin_memory() for b in batches]
+        ht = [torch.from_numpy(b.table_ids).pin_memory() for b in batches]
+        hg = torch.from_numpy(grad).pin_memory()
+        hout = [torch.empty((w.batch, w.total_dim), dtype=torch.float32).pin_memory() for _ in range(2)]
+        dbuf = [dict(k=torch.empty(max_nnz, dtype=torch.int64, device=dev), o=torch.empty_like(doffs[0]),
+                     t=torch.empty_like(dtids[0]), g=torch.empty_like(dgrad),
+                     out=torch.empty_like(out)) for _ in range(2)]
+        comp = torch.cuda.current_stream()
+        s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_up = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_down = [torch.cuda.Event() for _ in range(2)]
+
+        def upload(i):
+            b, k = i % 2, i % args.batches
+            n = hk[k].numel()
+            with torch.cuda.stream(s_up):
+                s_up.wait_event(ev_comp[b])          # step i-2 is done with these buffers
+                dbuf[b]["k"][:n].copy_(hk[k], non_blocking=True)
+                dbuf[b]["o"].copy_(ho[k], non_blocking=True)
+                dbuf[b]["t"].copy_(ht[k], non_blocking=True)
+                dbuf[b]["g"].copy_(hg, non_blocking=True)
+                ev_up[b].record(s_up)
+
+        def run_e2e(nsteps):
+            upload(0)
+            for i in range(nsteps):
+                b, k = i % 2, i % args.batches
+                n = hk[k].numel()
+                if i + 1 < nsteps:
+                    upload(i + 1)
+                comp.wait_event(ev_up[b])
+                comp.wait_event(ev_down[b])          # output buffer b has been read back
+                layer.forward(dbuf[b]["k"][:n], dbuf[b]["o"], dbuf[b]["t"], w.batch, dbuf[b]["out"])
+                layer.backward_update(dbuf[b]["g"], args.variant)
+                ev_comp[b].record(comp)
+                with torch.cuda.stream(s_down):
+                    s_down.wait_event(ev_comp[b])
+                    hout[b].copy_(dbuf[b]["out"], non_blocking=True)
+                    ev_down[b].record(s_down)
+            comp.wait_stream(s_down)
+
+        run_e2e(args.warmup)
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier(device_ids=[local])
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(comp)
+        run_e2e(args.steps)
+        f1.record(comp)
+        torch.cuda.synchronize()
+        ems = f0.elapsed_time(f1) / args.steps
+        if ws > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d = batches[0].keys.nbytes + batches[0].offsets.nbytes + batches[0].table_ids.nbytes + grad.nbytes
+        d2h = w.batch * w.total_dim * 4
+        e2e = {"value": ws * batches[0].nnz / (ems / 1e3), "unit": "lookups/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "copies": "pinned host <-> device, double-buffered on two copy streams overlapping compute"}
+
+    layer.close()
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+
+    nnz = batches[0].nnz
+    peak, peak_kind = _peaks()
+    per_phase_ms = {p: phases[p] / max(nsteps, 1) for p in phases}
+    dom = max(("forward", "reduce_update"), key=lambda p: per_phase_ms[p])
+    dom_kernel = {"forward": "fwd_pool", "reduce_update": "reduce_update_chunks+combine"}[dom]
+    dom_gbs = bytes_[dom] / (per_phase_ms[dom] / 1e3) / 1e9
+    step_gbs = bytes_["step"] / (ms / 1e3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic_%s_%s.json" % (args.config, args.variant))
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get(dom)
+
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        sw, sb, sg = cpu_sample(w, args.cpu_sample_batch)
+        import oracle
+        oracle.build()
+        secs = []
+        t_start = time.perf_counter()
+        while not secs or (time.perf_counter() - t_start < 10.0 and len(secs) < 20):
+            secs.append(oracle_step_timed(sw, sb, sg, w.seed))
+        cpu = {"value": sb.nnz / (sum(secs) / len(secs)), "unit": "lookups/s", "cores": 1, "kind": "oracle",
+               "sample": "%d of %d samples per table (%d lookups), full step a1..a5, mean of %d runs" % (
+                   args.cpu_sample_batch, w.batch, sb.nnz, len(secs))}
+
+    line = {
+        "metric": METRIC,
+        "value": ws * nnz / (ms / 1e3),
+        "unit": "lookups/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32" if all(s.dtype == "f32" for s in w.tables) else "f32-accumulate/16-bit-storage",
+        "data": "synthetic",
+        "config": {"workload": CONFIG_TEXT[args.config] + (
+                       " [batch overridden to %d]" % w.batch if args.batch else "") + (
+                       " [rows capped at %d]" % args.rows_cap if args.rows_cap else ""),
+                   "batch": w.batch, "nnz": nnz,
+                   "unique_rows": int(U_t.sum()), "variant": args.variant, "batches_cycled": args.batches,
+                   "l2": "inputs larger than L2 (tables %.1f GB; out, grad_out %.0f MB each)" % (
+                       sum(s.rows * s.dim * (_wbytes(s.dtype) + (4 if s.opt == "adagrad" else 0))
+                           for s in w.tables) / 1e9, w.batch * w.total_dim * 4 / 1e6),
+                   "parallelism": "replicas x%d" % ws},
+        "hbm": {"algorithmic_bytes_per_step": bytes_["step"], "achieved_gbs": step_gbs, "peak_gbs": peak,
+                "frac": step_gbs / peak, "peak_kind": peak_kind},
+        "phases_ms": per_phase_ms,
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": dom_gbs / peak, "traffic": traffic,
+                     "algorithmic_bytes": bytes_[dom], "peak_kind": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+// Internal declarations of the GB300 sparse embedding library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "emb.h"
+
+namespace emb {
+
+// ---------------------------------------------------------------------------
+// sticky device error bits (read and cleared by emb_sync_status)
+// ---------------------------------------------------------------------------
+enum : int {
+    ERRBIT_KEY_RANGE = 1,
+    ERRBIT_TABLE_ID = 2,
+    ERRBIT_CAPACITY = 4,
+    ERRBIT_TIMEOUT = 8,
+};
+
+constexpr int kMaxDim = 128;          // dims are multiples of 4 in [4, 128]
+constexpr int kMaxTables = 4096;
+constexpr uint32_t kEmptySlot = 0xFFFFFFFFu;
+constexpr uint32_t kNoSlot = 0xFFFFFFFEu;
+
+// Per-table metadata, resident in device memory.
+struct TableDev {
+    void* w;             // rows x dim, dtype
+    float* state;        // rows x dim fp32 (Adagrad) or null
+    int64_t rows;
+    uint32_t row_base;   // global row id of row 0
+    int32_t dim;
+    int32_t dtype;       // emb_dtype
+    int32_t pooling;     // emb_pooling
+    int32_t opt;         // emb_opt
+    float lr, eps;
+    int32_t doff;        // column offset in the concatenated output
+    int32_t pad_;
+};
+
+// ---------------------------------------------------------------------------
+// radix sort of (key, u32 value) pairs
+// ---------------------------------------------------------------------------
+constexpr int kSortThreads = 256;
+constexpr int kSortItemsSmall = 4;      // 1024-element tiles for n <= kSmallSortMax
+constexpr int kSortItemsLarge = 16;     // 4096-element tiles above
+constexpr int64_t kSmallSortMax = int64_t(8) << 20;
+constexpr int kMaxDigitBits = 10;
+
+struct SortPlan {
+    int64_t n_max;       // capacity in elements
+    int bits_max;        // keys < 2^bits_max
+    int digit_bits;      // D
+    int passes_max;      // ceil(bits_max / D)
+    int64_t tiles_max;
+    size_t counts_bytes; // [2^D][tiles] u32
+    size_t totals_bytes; // [2^D] u32
+};
+
+SortPlan make_sort_plan(int64_t n_max, int bits_max);
+
+// Sorts (keys_in, vals_in) ascending by key, stable, into (keys_out,
+// vals_out), using (keys_tmp, vals_tmp) as ping-pong space.  n is
+// n_dev ? *n_dev : n_host (n_host bounds the grid).  Only the low
+// bits_dev ? *bits_dev : plan.bits_max bits are sorted; at least one pass
+// always runs.  vals_in == nullptr means value = index.  key_sub (nullable,
+// 64-bit keys only) is subtracted from every input key first.
+// Returns the number of kernels launched, or -1 on a launch error.
+template <typename K>
+int radix_sort_pairs(const SortPlan& plan, const K* keys_in, const uint32_t* vals_in,
+                     K* keys_out, uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp,
+                     uint32_t* counts, uint32_t* totals, int64_t n_host, const int64_t* n_dev,
+                     const int32_t* bits_dev, const uint64_t* key_sub, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// run-length encoding of sorted keys (unique / counts / segment offsets)
+// ---------------------------------------------------------------------------
+constexpr int kRleThreads = 256;
+constexpr int kRleItems = 16;
+constexpr int kRleTile = kRleThreads * kRleItems;
+
+size_t rle_scratch_bytes(int64_t n_max);
+
+// From sorted keys sk[0..n): U runs of keys <= key_max.  Writes
+// unique[s] = sk + key_add (int64 or u32 output), seg_off[0..U], counts[0..U),
+// inverse[vals[p]] = s (or U for keys > key_max) when inverse != null,
+// *num_unique = U.  Returns kernels launched or -1.
+template <typename K>
+int rle_sorted(const K* sk, const uint32_t* vals, int64_t n, uint64_t key_max,
+               const uint64_t* key_add, int64_t* unique64, uint32_t* unique32,
+               int32_t* seg_off, int32_t* counts, int32_t* inverse, int64_t* num_unique,
+               void* scratch, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// kernels driven from layer.cu (defined in the other translation units)
+// ---------------------------------------------------------------------------
+struct ReduceArgs {
+    const uint32_t* skeys;      // sorted keys (global ids or unique indices)
+    const uint32_t* sbags;      // bag id per sorted position
+    int64_t n;
+    int64_t chunk;              // positions per warp
+    int64_t nchunks;
+    uint32_t key_limit;         // keys >= limit are skipped ...
+    const int64_t* key_limit_dev; // ... or >= *key_limit_dev when non-null
+    const uint32_t* gid_of_key; // null: key is the global id
+    const TableDev* tables;
+    int32_t num_tables;
+    int32_t batch;
+    const float* grad;
+    int64_t ld;
+    const float* bag_scale;
+    float* slots;               // [nchunks][2][kMaxDim]
+    uint32_t* split_list;       // [nchunks] chunks where a split run starts
+    int* split_count;
+    int* err;
+};
+
+int launch_reduce_update(const ReduceArgs& a, cudaStream_t st);   // returns kernels launched or -1
+
+struct FwdArgs {
+    const int64_t* keys;
+    const int64_t* offsets;
+    const int32_t* table_ids;
+    int32_t batch;
+    int32_t num_tables;
+    float* out;
+    int64_t ld;
+    const TableDev* tables;
+    uint32_t* gid_out;          // global row id per lookup (sentinel when skipped)
+    uint32_t* bag_out;          // bag id per lookup
+    float* bag_scale;           // 1/L per mean-pooled bag
+    uint32_t sentinel;          // = total rows: sorts after every valid id
+    int64_t warps_per_table;
+    int* err;
+};
+
+int launch_forward(const FwdArgs& a, cudaStream_t st);
+
+// dedup helpers (dedup.cu); each returns kernels launched or -1
+int launch_hash_insert(const uint32_t* gid, int64_t n, uint32_t limit, uint32_t* table, uint32_t mask,
+                       uint32_t* slot_of, uint32_t* ukey, uint32_t* uslot, int64_t* ucount, int* err,
+                       cudaStream_t st);
+int launch_hash_rank_inverse(const uint32_t* sslot, const int64_t* U_dev, uint32_t* slot_rank, int32_t* bits_dev,
+                             int32_t* seg_off, const uint32_t* slot_of, int64_t n, uint32_t* inv, cudaStream_t st);
+int launch_seg_from_sorted(const uint32_t* sk, int64_t n, const int64_t* U_dev, int32_t* seg_off, int32_t* counts,
+                           cudaStream_t st);
+int launch_hash_clear(uint32_t* table, const uint32_t* sslot, const int64_t* U_dev, int64_t n_max, cudaStream_t st);
+int launch_gather_u32(const uint32_t* src, const uint32_t* idx, int64_t n, uint32_t* dst, cudaStream_t st);
+int launch_minmax(const int64_t* keys, int64_t n, unsigned long long* mm, uint64_t* key_sub, int32_t* bits_dev,
+                  cudaStream_t st);
+
+}  // namespace emb

@@ -1,0 +1,212 @@
+// Forward: fused table lookup + pooling + concatenation.
+//
+// GTC 2022 "Merlin HugeCTR" slides, "COMMON EMBEDDING PRIMITIVES" and
+// "HUGECTR EMBEDDING LAYER": the lookup and the pooling are memory bound, so
+// lookup, in-register reduction and concatenation run as one kernel.  Merlin
+// overview article, section "HugeCTR": the vectors of one slot (bag) are
+// reduced to a single vector.
+//
+// Layout: bag j = t*B + b.  A warp owns 32 consecutive bags of one table,
+// split among groups of Lr = next_pow2(dim/4) lanes; each lane covers 4
+// columns (one 16-byte fp32 or 8-byte 16-bit load per row), and a group owns
+// Lr consecutive bags.  Because those bags are adjacent in the CSR, their
+// keys form one contiguous range, which the group streams through: keys are
+// loaded one per lane and broadcast inside the group, eight rows per lane are
+// kept in flight, and each bag's compensated fp32 sum is stored into its slice
+// of the concatenated output as soon as the stream passes the bag's end.  The same pass writes, for the
+// backward, the global row id (row_base + key) and the bag of every lookup,
+// and 1/L of every mean-pooled bag.
+#include "emb_internal.cuh"
+
+namespace emb {
+
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x)
+{
+    float y = __fsub_rn(x, c);
+    float t = __fadd_rn(s, y);
+    c = __fsub_rn(__fsub_rn(t, s), y);
+    s = t;
+}
+
+__device__ __forceinline__ float4 load_row4(const void* w, int dtype, int64_t elem)
+{
+    if (dtype == EMB_F32) return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(w) + elem));
+    uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(w) + elem));
+    if (dtype == EMB_F16) {
+        float2 fa = __half22float2(*reinterpret_cast<__half2*>(&raw.x));
+        float2 fb = __half22float2(*reinterpret_cast<__half2*>(&raw.y));
+        return make_float4(fa.x, fa.y, fb.x, fb.y);
+    }
+    float2 fa = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.x));
+    float2 fb = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.y));
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+
+constexpr int kPrefetch = 8;   // rows in flight per lane
+
+// Running state of a group streaming through its bags' keys.
+struct BagStream {
+    float4 s, c;        // compensated sum of the current bag (4 columns per lane)
+    int cur;            // current bag, index within the group
+    int64_t cur_end;    // its end offset
+};
+
+// Closes (scales and stores) every bag that ends at position `pos`, empty bags included.
+__device__ __forceinline__ void close_bags(BagStream& st, int64_t pos, int nbg, uint32_t gmask, int Lr, int my_len,
+                                           int64_t my_end, bool mean, bool colok, float* out_col, int64_t bg0,
+                                           int64_t ld)
+{
+    while (st.cur < nbg && st.cur_end == pos) {
+        const int L = __shfl_sync(gmask, my_len, st.cur, Lr);
+        float4 r = make_float4(__fsub_rn(st.s.x, st.c.x), __fsub_rn(st.s.y, st.c.y), __fsub_rn(st.s.z, st.c.z),
+                               __fsub_rn(st.s.w, st.c.w));
+        if (mean && L > 0) {
+            const float fl = (float)L;
+            r = make_float4(__fdiv_rn(r.x, fl), __fdiv_rn(r.y, fl), __fdiv_rn(r.z, fl), __fdiv_rn(r.w, fl));
+        }
+        if (colok) __stcs(reinterpret_cast<float4*>(out_col + (bg0 + st.cur) * ld), r);
+        st.s = make_float4(0.f, 0.f, 0.f, 0.f);
+        st.c = st.s;
+        ++st.cur;
+        const int64_t e = __shfl_sync(gmask, my_end, st.cur < nbg ? st.cur : 0, Lr);
+        st.cur_end = st.cur < nbg ? e : INT64_MAX;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) fwd_pool(FwdArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int t = (int)(gw / a.warps_per_table);
+    if (t >= a.num_tables) return;
+    const int64_t B = a.batch;
+    const TableDev tb = a.tables[t];
+    int Lr = 1;
+    while (Lr < ((tb.dim + 3) >> 2)) Lr <<= 1;
+    const int li = lane & (Lr - 1), g = lane / Lr;
+    const uint32_t gmask = Lr == 32 ? 0xffffffffu : (((1u << Lr) - 1u) << (g * Lr));
+    const bool colok = 4 * li < tb.dim;
+    const bool mean = tb.pooling == EMB_POOL_MEAN;
+
+    // this group owns bags bg0 .. bg0+nbg-1 of table t; lane li describes bag li
+    const int64_t bg0 = (gw - (int64_t)t * a.warps_per_table) * 32 + (int64_t)g * Lr;
+    const int64_t left = B - bg0;
+    const int nbg = left <= 0 ? 0 : (left < Lr ? (int)left : Lr);
+    if (nbg == 0) return;
+    const int64_t j0 = (int64_t)t * B + bg0;
+    const int64_t K0 = __ldg(a.offsets + j0);
+    int64_t my_end = INT64_MAX;
+    int my_len = 0;
+    bool my_tid_ok = true;
+    if (li < nbg) {
+        my_end = __ldg(a.offsets + j0 + li + 1);
+        my_tid_ok = __ldg(a.table_ids + j0 + li) == t;
+    }
+    int64_t my_start = __shfl_up_sync(gmask, my_end, 1, Lr);
+    if (li == 0) my_start = K0;
+    if (li < nbg) {
+        my_len = (int)(my_end - my_start);
+        if (!my_tid_ok) atomicOr(a.err, ERRBIT_TABLE_ID);
+        if (mean) a.bag_scale[j0 + li] = my_len > 0 ? __frcp_rn((float)my_len) : 0.f;
+    }
+    const int64_t K1 = __shfl_sync(gmask, my_end, nbg - 1, Lr);
+    float* const out_col = a.out + tb.doff + 4 * li;
+
+    if (__all_sync(gmask, li >= nbg || my_len == 1)) {
+        // one key per bag (one-hot feature): bag li is position K0 + li and
+        // its pooled value is the row itself, so rows go straight to the output
+        const int64_t i = K0 + li;
+        const bool in = li < nbg;
+        const int64_t key = in ? __ldg(a.keys + i) : 0;
+        const bool valid = in && my_tid_ok && key >= 0 && key < tb.rows;
+        if (in) {
+            a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
+            a.bag_out[i] = (uint32_t)(j0 + li);
+            if (!valid && my_tid_ok) atomicOr(a.err, ERRBIT_KEY_RANGE);
+        }
+        for (int q = 0; q < nbg; q += kPrefetch) {
+            float4 v[kPrefetch];
+#pragma unroll
+            for (int u = 0; u < kPrefetch; ++u) {
+                const int qq = q + u;
+                const int64_t kq = __shfl_sync(gmask, key, qq & (Lr - 1), Lr);
+                const bool vq = __shfl_sync(gmask, valid, qq & (Lr - 1), Lr) && qq < nbg;
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (vq && colok) v[u] = load_row4(tb.w, tb.dtype, kq * tb.dim + 4 * li);
+            }
+#pragma unroll
+            for (int u = 0; u < kPrefetch; ++u)
+                if (q + u < nbg && colok) __stcs(reinterpret_cast<float4*>(out_col + (bg0 + q + u) * a.ld), v[u]);
+        }
+        return;
+    }
+
+    BagStream st;
+    st.s = make_float4(0.f, 0.f, 0.f, 0.f);
+    st.c = st.s;
+    st.cur = 0;
+    st.cur_end = __shfl_sync(gmask, my_end, 0, Lr);
+#define CLOSE_BAGS(pos) close_bags(st, (pos), nbg, gmask, Lr, my_len, my_end, mean, colok, out_col, bg0, a.ld)
+
+    CLOSE_BAGS(K0);
+    for (int64_t base = K0; base < K1; base += Lr) {
+        const int64_t i = base + li;
+        const bool in = i < K1;
+        const int64_t key = in ? __ldg(a.keys + i) : 0;
+        // bag of position i = number of the group's bags that end at or before i
+        int k = 0;
+        for (int stp = Lr >> 1; stp > 0; stp >>= 1) {
+            const int64_t e = __shfl_sync(gmask, my_end, k + stp - 1, Lr);
+            if (e <= i) k += stp;
+        }
+        const bool tok = __shfl_sync(gmask, my_tid_ok, k, Lr);
+        const bool valid = in && tok && key >= 0 && key < tb.rows;
+        if (in) {
+            a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
+            a.bag_out[i] = (uint32_t)(j0 + k);
+            if (!valid && tok) atomicOr(a.err, ERRBIT_KEY_RANGE);
+        }
+        const int cnt = (int)((K1 - base) < Lr ? (K1 - base) : Lr);
+        for (int q = 0; q < cnt; q += kPrefetch) {
+            float4 v[kPrefetch];
+#pragma unroll
+            for (int u = 0; u < kPrefetch; ++u) {
+                const int qq = q + u;
+                const int64_t kq = __shfl_sync(gmask, key, qq & (Lr - 1), Lr);
+                const bool vq = __shfl_sync(gmask, valid, qq & (Lr - 1), Lr) && qq < cnt;
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (vq && colok) v[u] = load_row4(tb.w, tb.dtype, kq * tb.dim + 4 * li);
+            }
+#pragma unroll
+            for (int u = 0; u < kPrefetch; ++u) {
+                if (q + u < cnt) {
+                    kahan_add(st.s.x, st.c.x, v[u].x);
+                    kahan_add(st.s.y, st.c.y, v[u].y);
+                    kahan_add(st.s.z, st.c.z, v[u].z);
+                    kahan_add(st.s.w, st.c.w, v[u].w);
+                    CLOSE_BAGS(base + q + u + 1);
+                }
+            }
+        }
+    }
+    CLOSE_BAGS(K1);
+#undef CLOSE_BAGS
+}
+
+}  // namespace
+
+int launch_forward(const FwdArgs& a, cudaStream_t st)
+{
+    const int64_t warps = a.warps_per_table * a.num_tables;
+    if (warps <= 0) return 0;
+    const unsigned blocks = (unsigned)((warps * 32 + kThreads - 1) / kThreads);
+    fwd_pool<<<blocks, kThreads, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+}  // namespace emb

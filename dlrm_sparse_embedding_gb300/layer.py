@@ -1,0 +1,203 @@
+"""Thin Python binding over the C ABI: argument marshalling only.
+
+Tensors are torch CUDA tensors; every call runs on the current torch stream.
+All computation happens in libemb.so's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from ._lib import (DTYPES, OPTS, PHASES, POOLINGS, VARIANTS, EmbTableSpec, check, lib)
+
+_TORCH_WDTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+_NP_WDTYPE = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[ctypes.c_void_p]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _spec_field(s, name, default=None):
+    v = getattr(s, name, default)
+    return v if v is not None else default
+
+
+class EmbeddingLayer:
+    """Multi-table embedding layer resident on the current CUDA device.
+
+    ``tables``: sequence of objects with ``rows, dim`` and optionally
+    ``dtype`` ("f32"/"f16"/"bf16"), ``pooling`` ("sum"/"mean"), ``opt``
+    ("sgd"/"adagrad"), ``lr``, ``eps``, ``init_acc``.
+    """
+
+    def __init__(self, tables: Sequence, max_batch: int, max_nnz: int):
+        self.tables = list(tables)
+        T = len(self.tables)
+        arr = (EmbTableSpec * T)()
+        for i, s in enumerate(self.tables):
+            arr[i].rows = int(s.rows)
+            arr[i].dim = int(s.dim)
+            arr[i].dtype = DTYPES[_spec_field(s, "dtype", "f32")]
+            arr[i].pooling = POOLINGS[_spec_field(s, "pooling", "sum")]
+            arr[i].opt = OPTS[_spec_field(s, "opt", "sgd")]
+            arr[i].lr = float(_spec_field(s, "lr", 0.01))
+            arr[i].eps = float(_spec_field(s, "eps", 1e-8))
+            arr[i].init_acc = float(_spec_field(s, "init_acc", 0.0))
+        h = ctypes.c_void_p()
+        check(lib.emb_create(arr, T, int(max_batch), int(max_nnz), ctypes.byref(h)), "emb_create")
+        self._h = h
+        self.max_batch = int(max_batch)
+        self.max_nnz = int(max_nnz)
+        self.total_dim = sum(int(s.dim) for s in self.tables)
+        self.doff = np.concatenate([[0], np.cumsum([int(s.dim) for s in self.tables])[:-1]]).astype(np.int64)
+        self.row_base = np.concatenate([[0], np.cumsum([int(s.rows) for s in self.tables])[:-1]]).astype(np.int64)
+        self.last_nnz = 0
+
+    # -- life cycle ---------------------------------------------------------
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib.emb_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- step ---------------------------------------------------------------
+    def init_uniform(self, seed: int, lo: float, hi: float, stream=None) -> None:
+        check(lib.emb_init_uniform(self._h, ctypes.c_uint64(seed & (2 ** 64 - 1)), lo, hi, _stream(stream)),
+              "emb_init_uniform")
+
+    def forward(self, keys: torch.Tensor, offsets: torch.Tensor, table_ids: torch.Tensor, batch: int,
+                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty((batch, self.total_dim), dtype=torch.float32, device=offsets.device)
+        assert keys.dtype == torch.int64 and offsets.dtype == torch.int64 and table_ids.dtype == torch.int32
+        assert out.dtype == torch.float32 and out.shape == (batch, self.total_dim)
+        nnz = int(keys.numel())
+        check(lib.emb_forward(self._h, _ptr(keys) if nnz else None, _ptr(offsets), _ptr(table_ids), nnz,
+                              int(batch), _ptr(out), _stream(stream)), "emb_forward")
+        self.last_nnz = nnz
+        return out
+
+    def backward_update(self, grad_out: torch.Tensor, variant: str = "reduction", stream=None) -> None:
+        assert grad_out.dtype == torch.float32
+        check(lib.emb_backward_update(self._h, _ptr(grad_out), VARIANTS[variant], _stream(stream)),
+              "emb_backward_update")
+
+    # -- dedup by-products ----------------------------------------------------
+    def set_keep_dedup(self, keep: bool) -> None:
+        check(lib.emb_set_keep_dedup(self._h, 1 if keep else 0))
+
+    def dedup_result(self, with_inverse: bool = True, stream=None):
+        """(unique int64[U], inverse int32[nnz] or None, counts int32[U],
+        seg_offsets int32[U+1], sorted_bags int32[nnz]) of the last backward."""
+        n = max(self.last_nnz, 1)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        uniq = torch.empty(n, dtype=torch.int64, device=dev)
+        inv = torch.empty(n, dtype=torch.int32, device=dev) if with_inverse else None
+        cnt = torch.empty(n, dtype=torch.int32, device=dev)
+        seg = torch.empty(n + 1, dtype=torch.int32, device=dev)
+        bags = torch.empty(n, dtype=torch.int32, device=dev)
+        U = ctypes.c_int64()
+        check(lib.emb_dedup_result(self._h, _ptr(uniq), _ptr(inv), _ptr(cnt), _ptr(seg), _ptr(bags),
+                                   ctypes.byref(U), _stream(stream)), "emb_dedup_result")
+        u = U.value
+        m = self.last_nnz
+        return (uniq[:u], None if inv is None else inv[:m], cnt[:u], seg[:u + 1], bags[:m])
+
+    # -- rows -----------------------------------------------------------------
+    def gather_rows(self, t: int, rows: torch.Tensor, with_state: bool = False, stream=None):
+        spec = self.tables[t]
+        dt = _spec_field(spec, "dtype", "f32")
+        n = int(rows.numel())
+        w = torch.empty((n, int(spec.dim)), dtype=_TORCH_WDTYPE[dt], device=rows.device)
+        s = torch.empty((n, int(spec.dim)), dtype=torch.float32, device=rows.device) if with_state else None
+        check(lib.emb_gather_rows(self._h, t, _ptr(rows), n, _ptr(w), _ptr(s), _stream(stream)), "emb_gather_rows")
+        return w, s
+
+    def get_rows(self, t: int, row0: int, n: int, with_state: bool = False, stream=None):
+        spec = self.tables[t]
+        dt = _spec_field(spec, "dtype", "f32")
+        w = np.empty((n, int(spec.dim)), dtype=_NP_WDTYPE[dt])
+        s = np.empty((n, int(spec.dim)), dtype=np.float32) if with_state else None
+        check(lib.emb_get_rows(self._h, t, row0, n, w.ctypes.data_as(ctypes.c_void_p),
+                               None if s is None else s.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
+              "emb_get_rows")
+        return w, s
+
+    def set_rows(self, t: int, row0: int, weights: np.ndarray, state: Optional[np.ndarray] = None, stream=None):
+        spec = self.tables[t]
+        dt = _spec_field(spec, "dtype", "f32")
+        w = np.ascontiguousarray(weights, dtype=_NP_WDTYPE[dt])
+        s = None if state is None else np.ascontiguousarray(state, dtype=np.float32)
+        check(lib.emb_set_rows(self._h, t, row0, w.shape[0], w.ctypes.data_as(ctypes.c_void_p),
+                               None if s is None else s.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
+              "emb_set_rows")
+
+    # -- status ---------------------------------------------------------------
+    def sync_status(self, stream=None) -> int:
+        """Waits for the stream; returns and clears the sticky device status."""
+        return int(lib.emb_sync_status(self._h, _stream(stream)))
+
+    def set_timing(self, enable: bool) -> None:
+        check(lib.emb_set_timing(self._h, 1 if enable else 0), "emb_set_timing")
+
+    def phase_times(self, reset: bool = False):
+        """({phase: accumulated ms}, steps) of the steps timed since the last reset."""
+        arr = (ctypes.c_float * len(PHASES))()
+        steps = ctypes.c_int64()
+        check(lib.emb_phase_times(self._h, arr, len(PHASES), ctypes.byref(steps), 1 if reset else 0))
+        return {p: float(arr[i]) for i, p in enumerate(PHASES)}, steps.value
+
+    def launch_count(self, reset: bool = False) -> int:
+        c = ctypes.c_int64()
+        check(lib.emb_launch_count(self._h, ctypes.byref(c), 1 if reset else 0))
+        return c.value
+
+
+def unique_workspace_bytes(n: int) -> int:
+    b = ctypes.c_size_t()
+    check(lib.emb_unique_workspace(int(n), ctypes.byref(b)), "emb_unique_workspace")
+    return b.value
+
+
+def unique(keys: torch.Tensor, stream=None):
+    """Sorted unique keys, inverse index, counts and segment offsets of int64 keys.
+
+    Returns (unique[:U], inverse, counts[:U], seg_offsets[:U+1]); U is read
+    back to the host (one synchronisation)."""
+    assert keys.dtype == torch.int64 and keys.is_cuda
+    n = int(keys.numel())
+    dev = keys.device
+    m = max(n, 1)
+    uniq = torch.empty(m, dtype=torch.int64, device=dev)
+    inv = torch.empty(m, dtype=torch.int32, device=dev)
+    cnt = torch.empty(m, dtype=torch.int32, device=dev)
+    seg = torch.empty(m + 1, dtype=torch.int32, device=dev)
+    nu = torch.empty(1, dtype=torch.int64, device=dev)
+    ws_bytes = unique_workspace_bytes(n)
+    ws = torch.empty(ws_bytes + 256, dtype=torch.uint8, device=dev)
+    base = ws.data_ptr()
+    aligned = (base + 255) & ~255
+    check(lib.emb_unique(_ptr(keys) if n else None, n, _ptr(uniq), _ptr(inv), _ptr(cnt), _ptr(seg), _ptr(nu),
+                         ctypes.c_void_p(aligned), ws_bytes, _stream(stream)), "emb_unique")
+    U = int(nu.item())
+    return uniq[:U], inv[:n], cnt[:U], seg[:U + 1]

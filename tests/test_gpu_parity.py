@@ -1,0 +1,313 @@
+"""GPU vs oracle parity on small, several-tile workloads and edge cases.
+
+Every test calls the CUDA path through the C ABI (via the thin binding) and
+compares with the CPU oracle on the same seeded inputs: bit-exact for ids,
+counts, offsets and bag order; the stated relative tolerance for floats.
+"""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import ctr_inputs as ci
+import oracle
+from helpers import (TOL, bag_of_positions, expected_sorted_bags, gather_rows, init_rows_fn, max_rel_err,
+                     run_gpu_step)
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = ["reduction", "unique_sort", "unique_hash"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    import torch
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+
+
+def _small(name):
+    base = ci.workload(name if name in ci.WORKLOADS else name.split("_")[0])
+    if name == "tiny":
+        return base
+    if name == "dlrm_small":
+        tabs = tuple(ci.TableSpec(min(t.rows, 200_000), t.dim, t.dtype, t.pooling, t.opt, t.lr, t.eps)
+                     for t in base.tables)
+        return base.replace(name=name, tables=tabs, batch=4096)
+    if name == "multihot_small":
+        return base.replace(name=name, tables=base.tables[:10], batch=512).with_tables(rows=10_000)
+    if name == "multihot_bf16":
+        return base.replace(name=name, tables=base.tables[:6], batch=300).with_tables(rows=5_000, dtype="bf16")
+    if name == "huge_small":
+        return base.replace(name=name, batch=4096).with_tables(rows=1_000_000)
+    if name == "skew_small":
+        return base.replace(name=name, batch=2048).with_tables(rows=50_000)
+    raise KeyError(name)
+
+
+def check_step(w, batch, grad, variant, seed=0, expect_status=0, sample_untouched=64):
+    g = run_gpu_step(w, batch, grad, variant, seed, keep_layer=True)
+    layer = g.layer
+    try:
+        assert g.status_fwd == expect_status and g.status_bwd == 0
+        ref = oracle.step(w.tables, w.batch, batch.offsets, batch.keys, batch.table_ids, grad, init_rows_fn(w, seed))
+        # a1 forward
+        assert max_rel_err(g.out, ref.out, ref.out_scale) <= 1e-5
+        # a3 dedup: bit-exact
+        assert np.array_equal(g.unique, ref.unique)
+        assert np.array_equal(g.counts, ref.counts)
+        assert np.array_equal(g.seg_off, ref.seg_off)
+        if g.inverse is not None:
+            assert np.array_equal(g.inverse, ref.inverse)
+        exp_bags = expected_sorted_bags(ref.gids, bag_of_positions(batch.offsets))
+        assert np.array_equal(g.sorted_bags[:exp_bags.size], exp_bags)
+        # a5 updated rows, all touched rows
+        for t, spec in enumerate(w.tables):
+            sel = np.nonzero(ref.rows.table == t)[0]
+            if sel.size == 0:
+                continue
+            W, A = gather_rows(layer, w, t, ref.rows.row[sel])
+            idx = (ref.rows.row_start[sel][:, None] + np.arange(spec.dim)[None, :])
+            assert max_rel_err(W, ref.W[idx], ref.W_scale[idx]) <= TOL[spec.dtype], (t, spec)
+            if spec.opt == "adagrad":
+                assert max_rel_err(A, ref.A[idx], ref.A_scale[idx]) <= 1e-5, t
+        # untouched rows keep their initial values exactly
+        rng = np.random.default_rng(1)
+        for t, spec in enumerate(w.tables):
+            touched = set(ref.rows.row[ref.rows.table == t].tolist())
+            cand = rng.integers(0, spec.rows, size=sample_untouched)
+            rows = np.array([r for r in cand if r not in touched] + [spec.rows - 1] * (spec.rows - 1 not in touched),
+                            dtype=np.int64)
+            if rows.size == 0:
+                continue
+            W, A = gather_rows(layer, w, t, rows)
+            init = ci.stored_to_f64(ci.init_values(seed, t, rows, spec.dim, w.w_lo, w.w_hi, spec.dtype), spec.dtype)
+            assert np.array_equal(W, init)
+            if A is not None:
+                assert np.all(A == np.float32(spec.init_acc))
+        return g, ref
+    finally:
+        layer.close()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["tiny", "dlrm_small", "multihot_small", "multihot_bf16", "huge_small",
+                                  "skew_small"])
+def test_step_parity(name, variant):
+    w = _small(name)
+    batch = ci.make_batch(w)
+    grad = ci.make_grad(w)
+    check_step(w, batch, grad, variant)
+
+
+def test_init_matches_counter_generator_bit_exactly():
+    import torch
+    from dlrm_sparse_embedding_gb300 import EmbeddingLayer
+    tabs = [ci.TableSpec(3000, 16, "f32"), ci.TableSpec(777, 64, "f16", opt="adagrad", init_acc=0.1),
+            ci.TableSpec(5000, 128, "bf16")]
+    layer = EmbeddingLayer(tabs, 8, 16)
+    try:
+        layer.init_uniform(12345, -0.05, 0.05)
+        for t, s in enumerate(tabs):
+            W, A = layer.get_rows(t, 0, s.rows, with_state=s.opt == "adagrad")
+            ref = ci.init_values(12345, t, np.arange(s.rows), s.dim, -0.05, 0.05, s.dtype)
+            assert np.array_equal(W.view(np.uint16) if s.dtype != "f32" else W,
+                                  ref.view(np.uint16) if s.dtype == "f16" else ref)
+            if A is not None:
+                assert np.all(A == np.float32(0.1))
+    finally:
+        layer.close()
+
+
+# ---------------------------------------------------------------------------
+# unique primitive
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,lo,hi", [(0, 0, 1), (1, 5, 6), (7, -3, 3), (4096, 0, 100), (4097, -(1 << 40), 1 << 40),
+                                     (100_003, -(1 << 62), 1 << 62), (300_000, 0, 1_000), (65_536, 7, 8)])
+def test_unique_primitive_bit_exact(n, lo, hi):
+    import torch
+    from dlrm_sparse_embedding_gb300 import unique
+    rng = np.random.default_rng(n)
+    keys = rng.integers(lo, hi, size=n, dtype=np.int64)
+    u, inv, cnt, seg = unique(torch.from_numpy(keys).cuda())
+    ru, rinv, rcnt, rseg = oracle.unique(keys)
+    assert np.array_equal(u.cpu().numpy(), ru)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+    assert np.array_equal(cnt.cpu().numpy(), rcnt)
+    assert np.array_equal(seg.cpu().numpy(), rseg)
+
+
+def test_unique_extreme_int64_values():
+    import torch
+    from dlrm_sparse_embedding_gb300 import unique
+    keys = np.array([np.iinfo(np.int64).max, np.iinfo(np.int64).min, 0, -1, np.iinfo(np.int64).max, 1],
+                    dtype=np.int64)
+    u, inv, cnt, seg = unique(torch.from_numpy(keys).cuda())
+    ru, rinv, rcnt, rseg = oracle.unique(keys)
+    assert np.array_equal(u.cpu().numpy(), ru) and np.array_equal(inv.cpu().numpy(), rinv)
+    assert np.array_equal(cnt.cpu().numpy(), rcnt) and np.array_equal(seg.cpu().numpy(), rseg)
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+
+def _custom(tables, B, lens, key_fn, seed=0, name="edge"):
+    w = ci.Workload(name=name, tables=tuple(tables), batch=B, hot_kind="fixed", hot_lo=1, hot_hi=1,
+                    key_dist="uniform", seed=seed)
+    lens = np.asarray(lens, dtype=np.int64).reshape(-1)
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    keys = np.empty(int(offsets[-1]), dtype=np.int64)
+    rng = np.random.default_rng(seed)
+    for j in range(len(tables) * B):
+        t = j // B
+        keys[offsets[j]:offsets[j + 1]] = key_fn(rng, t, tables[t], int(lens[j]))
+    batch = ci.Batch(keys=keys, offsets=offsets, table_ids=np.repeat(np.arange(len(tables), dtype=np.int32), B),
+                     batch=B)
+    grad = np.random.default_rng(seed + 1).standard_normal((B, sum(t.dim for t in tables))).astype(np.float32)
+    return w, batch, grad
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_empty_bags_and_mean_pooling(variant):
+    tabs = [ci.TableSpec(500, 16, pooling="mean", opt="adagrad"), ci.TableSpec(300, 32, pooling="sum")]
+    lens = np.random.default_rng(3).integers(0, 4, size=2 * 200)
+    lens[:17] = 0
+    w, b, g = _custom(tabs, 200, lens, lambda rng, t, s, L: rng.integers(0, s.rows, L))
+    check_step(w, b, g, variant)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_zero_lookups(variant):
+    tabs = [ci.TableSpec(50, 8)]
+    w, b, g = _custom(tabs, 16, np.zeros(16), lambda rng, t, s, L: np.zeros(0, np.int64))
+    gs = run_gpu_step(w, b, g, variant)
+    assert np.all(gs.out == 0) and gs.unique.size == 0 and gs.seg_off.tolist() == [0]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_one_key_everywhere_spans_many_chunks(variant):
+    # every lookup hits row 7: one run crossing every chunk boundary
+    tabs = [ci.TableSpec(1000, 64, opt="adagrad"), ci.TableSpec(10, 128)]
+    w, b, g = _custom(tabs, 5000, np.full(2 * 5000, 30), lambda rng, t, s, L: np.full(L, 7 if t == 0 else s.rows - 1))
+    check_step(w, b, g, variant)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_odd_dims_and_last_rows(variant):
+    dims = [4, 12, 48, 100, 128, 20]
+    tabs = [ci.TableSpec(r, d, opt="adagrad" if i % 2 else "sgd", pooling="mean" if i % 3 == 0 else "sum")
+            for i, (r, d) in enumerate(zip([3, 64, 1000, 17, 5, 2], dims))]
+    lens = np.random.default_rng(5).integers(0, 9, size=len(tabs) * 333)
+    w, b, g = _custom(tabs, 333, lens,
+                      lambda rng, t, s, L: np.where(rng.random(L) < 0.3, s.rows - 1, rng.integers(0, s.rows, L)))
+    check_step(w, b, g, variant)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_out_of_range_keys_are_skipped_and_reported(variant):
+    from dlrm_sparse_embedding_gb300 import EMB_ERR_KEY_RANGE
+    tabs = [ci.TableSpec(100, 16), ci.TableSpec(40, 32, opt="adagrad")]
+
+    def keys(rng, t, s, L):
+        k = rng.integers(0, s.rows, L)
+        bad = rng.random(L) < 0.1
+        k[bad] = rng.choice([-1, s.rows, s.rows + 5, -(1 << 40), 1 << 40], size=int(bad.sum()))
+        return k
+
+    w, b, g = _custom(tabs, 256, np.random.default_rng(2).integers(1, 6, 512), keys)
+    check_step(w, b, g, variant, expect_status=EMB_ERR_KEY_RANGE)
+
+
+def test_wrong_table_id_is_reported():
+    import torch
+    from dlrm_sparse_embedding_gb300 import EMB_ERR_INVALID_ARG, EmbeddingLayer
+    tabs = [ci.TableSpec(100, 16), ci.TableSpec(40, 16)]
+    w, b, g = _custom(tabs, 64, np.ones(128), lambda rng, t, s, L: rng.integers(0, s.rows, L))
+    b.table_ids[70] = 0
+    layer = EmbeddingLayer(tabs, 64, b.nnz)
+    try:
+        layer.init_uniform(0, -0.05, 0.05)
+        out = layer.forward(torch.from_numpy(b.keys).cuda(), torch.from_numpy(b.offsets).cuda(),
+                            torch.from_numpy(b.table_ids).cuda(), 64)
+        assert layer.sync_status() == EMB_ERR_INVALID_ARG
+        ref = oracle.step(tabs, 64, b.offsets, b.keys, b.table_ids, g, init_rows_fn(w, 0))
+        assert max_rel_err(out.cpu().numpy(), ref.out, ref.out_scale) <= 1e-5
+    finally:
+        layer.close()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_deterministic_bitwise(variant):
+    w = _small("skew_small").replace(batch=512)
+    batch = ci.make_batch(w)
+    grad = ci.make_grad(w)
+    outs = []
+    for _ in range(2):
+        gs = run_gpu_step(w, batch, grad, variant, keep_layer=True)
+        rows = []
+        for t in range(w.num_tables):
+            W, _ = gs.layer.get_rows(t, 0, 64)
+            rows.append(W.copy())
+        gs.layer.close()
+        outs.append((gs.out, rows))
+    assert np.array_equal(outs[0][0], outs[1][0])
+    for a, c in zip(outs[0][1], outs[1][1]):
+        assert np.array_equal(a, c)
+
+
+def test_variants_agree():
+    w = _small("multihot_small")
+    batch = ci.make_batch(w)
+    grad = ci.make_grad(w)
+    res = {}
+    for v in VARIANTS:
+        gs = run_gpu_step(w, batch, grad, v, keep_layer=True)
+        res[v] = (gs.unique, gs.counts, gs.seg_off, gs.sorted_bags,
+                  [gs.layer.get_rows(t, 0, 2000, with_state=True) for t in range(3)])
+        gs.layer.close()
+    for v in VARIANTS[1:]:
+        for a, c in zip(res["reduction"][:4], res[v][:4]):
+            assert np.array_equal(a, c)
+        for (wa, sa), (wc, sc) in zip(res["reduction"][4], res[v][4]):
+            assert np.array_equal(wa, wc) and np.array_equal(sa, sc)
+
+
+def test_backward_before_forward_is_a_state_error():
+    import torch
+    from dlrm_sparse_embedding_gb300 import EMB_ERR_STATE, EmbError, EmbeddingLayer
+    layer = EmbeddingLayer([ci.TableSpec(10, 8)], 4, 4)
+    try:
+        with pytest.raises(EmbError) as e:
+            layer.backward_update(torch.zeros((4, 8), device="cuda"))
+        assert e.value.status == EMB_ERR_STATE
+    finally:
+        layer.close()
+
+
+def test_allocation_failure_returns_oom_and_leaks_nothing():
+    code = (
+        "import ctypes, torch, sys; sys.path.insert(0, %r)\n"
+        "from dlrm_sparse_embedding_gb300 import EmbeddingLayer, EmbError, EMB_ERR_OOM\n"
+        "import ctr_inputs as ci\n"
+        "torch.cuda.init()\n"
+        "free0 = torch.cuda.mem_get_info()[0]\n"
+        "try:\n"
+        "    EmbeddingLayer([ci.TableSpec(1000000, 64)] * 4, 1024, 100000)\n"
+        "    print('NO-ERROR')\n"
+        "except EmbError as e:\n"
+        "    assert e.status == EMB_ERR_OOM, e.status\n"
+        "    torch.cuda.synchronize()\n"
+        "    print('OOM', free0 - torch.cuda.mem_get_info()[0])\n"
+    ) % os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, EMB_TEST_ALLOC_LIMIT_BYTES=str(600 << 20))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.startswith("OOM"), r.stdout
+    leaked = int(r.stdout.split()[1])
+    assert leaked < (64 << 20)

@@ -141,6 +141,22 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
+def max_over_ranks(value: float, device) -> float:
+    """Largest value over all ranks (each rank times its own replica)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world_size: int, ms_per_step_max: float) -> float:
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return world_size * units_per_rank / (ms_per_step_max / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -292,10 +308,7 @@ def main():
     launches = layer.launch_count(reset=True)
     layer.set_timing(False)
     status = layer.sync_status()
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
 
     # ---- end to end: host buffers, copies inside the timed region ----
     # Every step copies its inputs (keys, offsets, table ids, grad_out) from
@@ -357,13 +370,10 @@ def main():
         f1.record(comp)
         torch.cuda.synchronize()
         ems = f0.elapsed_time(f1) / args.steps
-        if ws > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(ems, dev)
         h2d = batches[0].keys.nbytes + batches[0].offsets.nbytes + batches[0].table_ids.nbytes + grad.nbytes
         d2h = w.batch * w.total_dim * 4
-        e2e = {"value": ws * batches[0].nnz / (ems / 1e3), "unit": "lookups/s", "ms_per_step": ems,
+        e2e = {"value": whole_job_rate(batches[0].nnz, ws, ems), "unit": "lookups/s", "ms_per_step": ems,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "copies": "pinned host <-> device, double-buffered on two copy streams overlapping compute"}
 
@@ -401,7 +411,7 @@ def main():
 
     line = {
         "metric": METRIC,
-        "value": ws * nnz / (ms / 1e3),
+        "value": whole_job_rate(nnz, ws, ms),
         "unit": "lookups/s",
         "n_gpus": ws,
         "steps": args.steps,

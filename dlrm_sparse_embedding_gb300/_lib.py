@@ -30,8 +30,9 @@ EXPORTS = (
     "emb_create", "emb_destroy", "emb_init_uniform", "emb_forward", "emb_backward_update",
     "emb_set_keep_dedup", "emb_dedup_result", "emb_unique_workspace", "emb_unique",
     "emb_get_rows", "emb_set_rows", "emb_gather_rows", "emb_sync_status", "emb_launch_count",
-    "emb_set_timing", "emb_phase_times", "emb_status_string",
+    "emb_set_timing", "emb_phase_times", "emb_unique_noalloc", "emb_status_string",
 )
+UNIQUE_NOALLOC_MAX_KEYS = 262144
 PHASES = ("forward", "dedup", "reduce_update")
 
 
@@ -69,6 +70,7 @@ def _load() -> ctypes.CDLL:
     L.emb_dedup_result.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.POINTER(i64), vp]
     L.emb_unique_workspace.argtypes = [i64, ctypes.POINTER(ctypes.c_size_t)]
     L.emb_unique.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    L.emb_unique_noalloc.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp]
     L.emb_get_rows.argtypes = [vp, i32, i64, i64, vp, vp, vp]
     L.emb_set_rows.argtypes = [vp, i32, i64, i64, vp, vp, vp]
     L.emb_gather_rows.argtypes = [vp, i32, vp, i64, vp, vp, vp]

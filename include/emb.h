@@ -167,6 +167,28 @@ int emb_unique(const int64_t* keys, int64_t n, int64_t* unique, int32_t* inverse
                int32_t* counts, int32_t* seg_offsets, int64_t* num_unique,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/* emb_unique without any allocation, for callers that cannot allocate device
+ * memory at call time: for instance a plugin whose enqueue path runs inside a
+ * host framework that forbids cudaMalloc there (it may synchronise the device,
+ * and fails outright under a fixed memory budget), or a serving thread that
+ * must not touch the allocator while requests are in flight.  There is no
+ * counterpart on the pages: this is a library convenience, not part of the
+ * embedding method.
+ *
+ * Arguments and results are exactly those of emb_unique, minus the workspace:
+ * the scratch is one array compiled into the library (about 9 MB of device
+ * memory, held on every GPU that loads the library until the process exits).
+ * n must be at most EMB_UNIQUE_NOALLOC_MAX_KEYS; larger n returns
+ * EMB_ERR_INVALID_ARG and enqueues nothing.  The first call on a device looks
+ * up the array's address on that device (the device current at the call), so
+ * make that first call before any stream capture.  All calls share the one
+ * array: calls whose GPU work overlaps -- on different streams or from
+ * different threads without ordering -- race on it and give wrong results; the
+ * contents left by the previous call are never relied on. */
+#define EMB_UNIQUE_NOALLOC_MAX_KEYS 262144
+int emb_unique_noalloc(const int64_t* keys, int64_t n, int64_t* unique, int32_t* inverse,
+                       int32_t* counts, int32_t* seg_offsets, int64_t* num_unique, void* stream);
+
 /* Copy rows [row0, row0+n) of table t between the layer and host memory.
  * weights_host holds n*dim values of the table dtype (fp32, or the raw 16-bit
  * patterns of fp16/bf16); state_host (nullable; Adagrad tables only) n*dim

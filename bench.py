@@ -392,9 +392,15 @@ def main():
     step_gbs = bytes_["step"] / (ms / 1e3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic_%s_%s.json" % (args.config, args.variant))
-    if os.path.exists(tpath):
+    if os.path.exists(tpath) and not (args.batch or args.rows_cap):
+        # ncu DRAM bytes of the dominant phase, valid only while its kernel source is unchanged
         with open(tpath) as f:
-            traffic = json.load(f).get(dom)
+            rec = json.load(f).get(dom)
+        if rec:
+            import hashlib
+            with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() == rec["source_sha256"]:
+                    traffic = rec["traffic_bytes"]
 
     cpu = None
     if not args.no_cpu_baseline and ws == 1:

@@ -46,7 +46,7 @@ struct TableDev {
 // ---------------------------------------------------------------------------
 constexpr int kSortThreads = 256;
 constexpr int kSortItemsSmall = 4;      // 1024-element tiles for n <= kSmallSortMax
-constexpr int kSortItemsLarge = 16;     // 4096-element tiles above
+constexpr int kSortItemsLarge = 8;      // 2048-element tiles above
 constexpr int64_t kSmallSortMax = int64_t(8) << 20;
 constexpr int kMaxDigitBits = 10;
 
@@ -56,8 +56,8 @@ struct SortPlan {
     int digit_bits;      // D
     int passes_max;      // ceil(bits_max / D)
     int64_t tiles_max;
-    size_t counts_bytes; // [2^D][tiles] u32
-    size_t totals_bytes; // [2^D] u32
+    size_t desc_bytes;   // look-back descriptors [tiles][2^D] u64
+    size_t aux_bytes;    // histograms [passes][2^D] + tile counters [passes] u32
 };
 
 SortPlan make_sort_plan(int64_t n_max, int bits_max);
@@ -69,11 +69,14 @@ SortPlan make_sort_plan(int64_t n_max, int bits_max);
 // always runs.  vals_in == nullptr means value = index.  key_sub (nullable,
 // 64-bit keys only) is subtracted from every input key first.
 // Returns the number of kernels launched, or -1 on a launch error.
+// `desc` (plan.desc_bytes, zeroed once when allocated) and `aux`
+// (plan.aux_bytes) are scratch; a look-back that gives up sets
+// ERRBIT_TIMEOUT in *err.
 template <typename K>
 int radix_sort_pairs(const SortPlan& plan, const K* keys_in, const uint32_t* vals_in,
                      K* keys_out, uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp,
-                     uint32_t* counts, uint32_t* totals, int64_t n_host, const int64_t* n_dev,
-                     const int32_t* bits_dev, const uint64_t* key_sub, cudaStream_t st);
+                     uint64_t* desc, uint32_t* aux, int64_t n_host, const int64_t* n_dev,
+                     const int32_t* bits_dev, const uint64_t* key_sub, int* err, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // run-length encoding of sorted keys (unique / counts / segment offsets)
@@ -87,12 +90,13 @@ size_t rle_scratch_bytes(int64_t n_max);
 // From sorted keys sk[0..n): U runs of keys <= key_max.  Writes
 // unique[s] = sk + key_add (int64 or u32 output), seg_off[0..U], counts[0..U),
 // inverse[vals[p]] = s (or U for keys > key_max) when inverse != null,
-// *num_unique = U.  Returns kernels launched or -1.
+// *num_unique = U, or -1 when *err (nullable) is set by the sort before it.
+// Returns kernels launched or -1.
 template <typename K>
 int rle_sorted(const K* sk, const uint32_t* vals, int64_t n, uint64_t key_max,
                const uint64_t* key_add, int64_t* unique64, uint32_t* unique32,
                int32_t* seg_off, int32_t* counts, int32_t* inverse, int64_t* num_unique,
-               void* scratch, cudaStream_t st);
+               void* scratch, const int* err, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // kernels driven from layer.cu (defined in the other translation units)
@@ -101,8 +105,9 @@ struct ReduceArgs {
     const uint32_t* skeys;      // sorted keys (global ids or unique indices)
     const uint32_t* sbags;      // bag id per sorted position
     int64_t n;
-    int64_t chunk;              // positions per warp
+    int64_t chunk;              // nominal positions per warp (starts snap to run starts)
     int64_t nchunks;
+    int32_t lanes_per_row;      // Lg: lanes sharing one row, one float4 column each (power of two, 4*Lg >= max dim)
     uint32_t key_limit;         // keys >= limit are skipped ...
     const int64_t* key_limit_dev; // ... or >= *key_limit_dev when non-null
     const uint32_t* gid_of_key; // null: key is the global id

@@ -49,6 +49,14 @@ __device__ __forceinline__ float4 load_row4(const void* w, int dtype, int64_t el
 
 constexpr int kPrefetch = 8;   // rows in flight per lane
 
+// Asks L2 for the whole row (at most 512 bytes = 4 lines) of one key.
+__device__ __forceinline__ void prefetch_row_l2(const TableDev& tb, int64_t key)
+{
+    const int wb = tb.dtype == EMB_F32 ? 4 : 2;
+    const char* p = static_cast<const char*>(tb.w) + key * tb.dim * wb;
+    for (int off = 0; off < tb.dim * wb; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+}
+
 // Running state of a group streaming through its bags' keys.
 struct BagStream {
     float4 s, c;        // compensated sum of the current bag (4 columns per lane)
@@ -124,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_pool(FwdArgs a)
         const bool in = li < nbg;
         const int64_t key = in ? __ldg(a.keys + i) : 0;
         const bool valid = in && my_tid_ok && key >= 0 && key < tb.rows;
+        if (valid) prefetch_row_l2(tb, key);
         if (in) {
             a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
             a.bag_out[i] = (uint32_t)(j0 + li);

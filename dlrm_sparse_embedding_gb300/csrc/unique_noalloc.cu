@@ -13,7 +13,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(9) << 20;   // fits emb_unique's workspace for the maximum n
+constexpr size_t kNoAllocScratchBytes = size_t(12) << 20;  // fits emb_unique's workspace for the maximum n
 constexpr int kMaxDevices = 64;
 
 // The scratch.  Host code must not use this name as an address: on the host it

@@ -12,14 +12,23 @@
 // storage of the GTC 2022 HugeCTR slides (slide "WEIGHT CONVERSION FOR MIXED
 // PRECISION TRAINING").
 //
-// Work split: one warp per chunk of `chunk` consecutive sorted lookups.  A run
-// that lies inside one chunk is reduced and applied by that warp.  A run that
-// crosses chunk boundaries is cut into pieces; each chunk writes its piece's
-// partial sum into a per-chunk slot, the chunk where the run starts registers
-// it in a compact list, and a second kernel (persistent blocks over that list)
-// adds the pieces in chunk order and applies the update.  Every sum is a
-// compensated (Kahan) fp32 sum in a fixed order, so results are deterministic
-// and independent of scheduling; there are no atomics on the data path.
+// Work split: one warp per chunk of about `chunk` consecutive sorted lookups;
+// each chunk boundary snaps forward to the next run start within `chunk`
+// lookups, so only runs longer than a chunk are ever cut.  The warp lists the
+// runs of its chunk in shared memory together with the bag of every lookup;
+// lane groups of Lg = next_pow2(dim/4) lanes (one float4 column each) take
+// runs round-robin, so dims below 128 have several runs in flight per warp,
+// and every group asks L2 for the rows of the runs two steps ahead (table row,
+// accumulator, first gradient rows) while it reduces the current one.  A run
+// inside the chunk is reduced and applied by its group; its table row and
+// accumulator are loaded when the run starts, overlapping the gradient
+// gathers.  A run that crosses chunk boundaries is cut into
+// pieces; each chunk writes its piece's partial sum into a per-chunk slot, the
+// chunk where the run starts registers it in a compact list, and a second
+// kernel (persistent blocks over that list) adds the pieces in chunk order and
+// applies the update.  Every sum is a compensated (Kahan) fp32 sum in a fixed
+// order, so results are deterministic and independent of scheduling; there are
+// no atomics on values.
 #include "emb_internal.cuh"
 
 namespace emb {
@@ -34,14 +43,6 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x)
     float t = __fadd_rn(s, y);
     c = __fsub_rn(__fsub_rn(t, s), y);
     s = t;
-}
-
-__device__ __forceinline__ int lanes_for_dim(int d)
-{
-    int l = (d + 3) >> 2;
-    int p = 1;
-    while (p < l) p <<= 1;
-    return p;
 }
 
 __device__ __forceinline__ float4 load_w4(const void* w, int dtype, int64_t elem)
@@ -108,168 +109,186 @@ __device__ __forceinline__ float* slot_ptr(float* slots, int64_t chunk, int whic
 
 enum { kSlotHead = 0, kSlotTail = 1 };
 
-struct RunState {
-    uint32_t key;
-    bool open;
-    bool started_before;
-    int t;
-    TableDev tb;
-    int Lr, G, li, g;
-    int64_t elem;        // first element of this lane's 4 columns in the row
-    float4 w, a;         // row values (and accumulator) loaded when the run opens
-    float s[4], c[4];
-};
-
 __device__ __forceinline__ float4 load_state4(const TableDev& tb, int64_t elem)
 {
     if (tb.opt != EMB_OPT_ADAGRAD) return make_float4(0.f, 0.f, 0.f, 0.f);
     return *reinterpret_cast<const float4*>(tb.state + elem);
 }
 
-__device__ __forceinline__ void open_run(RunState& r, const ReduceArgs& a, uint32_t key, uint32_t bag0,
-                                         bool started_before, int lane)
+// Snapped chunk start: the first run start in [c*chunk, c*chunk + chunk), or
+// c*chunk itself when a run covers that whole window.  Whole warp.
+__device__ __forceinline__ int64_t chunk_start(const ReduceArgs& a, int64_t c, int lane)
 {
-    r.key = key;
-    r.open = true;
-    r.started_before = started_before;
-    r.t = (int)(bag0 / (uint32_t)a.batch);
-    r.tb = a.tables[r.t];
-    r.Lr = lanes_for_dim(r.tb.dim);
-    r.G = 32 / r.Lr;
-    r.li = lane & (r.Lr - 1);
-    r.g = lane / r.Lr;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) { r.s[q] = 0.f; r.c[q] = 0.f; }
-    // A run that starts in this chunk will most likely be applied here: fetch
-    // its row now so the load overlaps the gradient gathers.
-    if (!started_before && r.g == 0 && 4 * r.li < r.tb.dim) {
-        const uint32_t gid = a.gid_of_key ? a.gid_of_key[key] : key;
-        r.elem = (int64_t)(gid - r.tb.row_base) * r.tb.dim + 4 * r.li;
-        r.w = load_w4(r.tb.w, r.tb.dtype, r.elem);
-        r.a = load_state4(r.tb, r.elem);
+    if (c <= 0) return 0;
+    const int64_t base = c * a.chunk;
+    if (base >= a.n) return a.n;
+    const int64_t lim = base + a.chunk < a.n ? base + a.chunk : a.n;
+    for (int64_t w = base; w < lim; w += 32) {
+        const int64_t p = w + lane;
+        bool head = false;
+        if (p < lim) head = a.skeys[p] != a.skeys[p - 1];
+        const uint32_t m = __ballot_sync(0xffffffffu, head);
+        if (m) return w + __ffs(m) - 1;
     }
+    return base;
 }
 
-// Adds the grad rows of lookups [x0, x1) of the current window (lane-indexed
-// bag ids in `bg`) to the open run.
-__device__ __forceinline__ void accumulate(RunState& r, const ReduceArgs& a, uint32_t bg, int x0, int x1)
+__device__ __forceinline__ void prefetch_l2(const void* p)
 {
-    const bool colok = 4 * r.li < r.tb.dim;
-    const bool mean = r.tb.pooling == EMB_POOL_MEAN;
-    const uint32_t tB = (uint32_t)r.t * (uint32_t)a.batch;
-    for (int x = x0; x < x1; x += 2 * r.G) {
-        const int xa = x + r.g, xb = x + r.G + r.g;
-        const uint32_t ba = __shfl_sync(0xffffffffu, bg, xa < 32 ? xa : 0);
-        const uint32_t bb = __shfl_sync(0xffffffffu, bg, xb < 32 ? xb : 0);
-        const bool va = xa < x1 && colok, vb = xb < x1 && colok;
-        float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), gb = ga;
-        float sa = 1.f, sb = 1.f;
-        if (va) {
-            ga = __ldg(reinterpret_cast<const float4*>(a.grad + (int64_t)(ba - tB) * a.ld + r.tb.doff) + r.li);
-            if (mean) sa = __ldg(a.bag_scale + ba);
-        }
-        if (vb) {
-            gb = __ldg(reinterpret_cast<const float4*>(a.grad + (int64_t)(bb - tB) * a.ld + r.tb.doff) + r.li);
-            if (mean) sb = __ldg(a.bag_scale + bb);
-        }
-        if (va) {
-            kahan_add(r.s[0], r.c[0], mean ? __fmul_rn(ga.x, sa) : ga.x);
-            kahan_add(r.s[1], r.c[1], mean ? __fmul_rn(ga.y, sa) : ga.y);
-            kahan_add(r.s[2], r.c[2], mean ? __fmul_rn(ga.z, sa) : ga.z);
-            kahan_add(r.s[3], r.c[3], mean ? __fmul_rn(ga.w, sa) : ga.w);
-        }
-        if (vb) {
-            kahan_add(r.s[0], r.c[0], mean ? __fmul_rn(gb.x, sb) : gb.x);
-            kahan_add(r.s[1], r.c[1], mean ? __fmul_rn(gb.y, sb) : gb.y);
-            kahan_add(r.s[2], r.c[2], mean ? __fmul_rn(gb.z, sb) : gb.z);
-            kahan_add(r.s[3], r.c[3], mean ? __fmul_rn(gb.w, sb) : gb.w);
-        }
-    }
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// Closes the open run: reduce across lane groups, then update the row or
-// store the piece into the chunk's slot.
-__device__ __forceinline__ void finalize(RunState& r, const ReduceArgs& a, int64_t chunk, bool extends_after)
+// Asks L2 for every 128-byte line of `bytes` bytes at p, spread over the
+// group's lanes (rows are at most 512 bytes: at most 4 lines).
+__device__ __forceinline__ void prefetch_row(const void* p, int bytes, int li, int Lg)
 {
-    for (int off = r.Lr; off < 32; off <<= 1) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float os = __shfl_xor_sync(0xffffffffu, r.s[q], off);
-            float oc = __shfl_xor_sync(0xffffffffu, r.c[q], off);
-            kahan_add(r.s[q], r.c[q], os);
-            kahan_add(r.s[q], r.c[q], -oc);
-        }
-    }
-    float gsum[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) gsum[q] = __fsub_rn(r.s[q], r.c[q]);
-    if (r.g == 0 && 4 * r.li < r.tb.dim) {
-        if (r.started_before || extends_after) {
-            float* sp = slot_ptr(a.slots, chunk, r.started_before ? kSlotHead : kSlotTail);
-            *reinterpret_cast<float4*>(sp + 4 * r.li) = make_float4(gsum[0], gsum[1], gsum[2], gsum[3]);
-            // the chunk where a split run starts registers it for the combine kernel
-            if (!r.started_before && r.li == 0) a.split_list[atomicAdd(a.split_count, 1)] = (uint32_t)chunk;
-        } else {
-            apply_update4(r.tb, r.elem, gsum, r.w, r.a);
-        }
-    }
-    r.open = false;
+    const char* c = static_cast<const char*>(p);
+    for (int off = li * 128; off < bytes; off += Lg * 128) prefetch_l2(c + off);
 }
 
-__global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a)
+constexpr int kPrefetchRows = 8;   // gradient rows of a future run asked for ahead of time
+
+// Issues L2 prefetches for run r (its table row, accumulator and first
+// gradient rows) so they are on chip when the group reaches it.
+__device__ __forceinline__ void prefetch_run(const ReduceArgs& a, const uint32_t* runs, const uint32_t* rkeys,
+                                             const uint32_t* bags, int r, int R, bool first_before, bool last_after,
+                                             uint32_t limit, int li, int Lg)
 {
-    const int lane = threadIdx.x & 31;
+    if (r >= R) return;
+    const uint32_t key = rkeys[r];
+    if (key >= limit) return;
+    const uint32_t s0 = runs[r], s1 = runs[r + 1];
+    const uint32_t bag0 = bags[s0];
+    const int t = (int)(bag0 / (uint32_t)a.batch);
+    const TableDev& tb = a.tables[t];
+    const int rowf = tb.dim * 4;
+    const uint32_t tB = (uint32_t)t * (uint32_t)a.batch;
+    if (!(r == 0 && first_before) && !(r == R - 1 && last_after)) {
+        const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
+        const int64_t elem = (int64_t)(gid - tb.row_base) * tb.dim;
+        const int wb = tb.dtype == EMB_F32 ? 4 : 2;
+        prefetch_row(static_cast<const char*>(tb.w) + elem * wb, tb.dim * wb, li, Lg);
+        if (tb.opt == EMB_OPT_ADAGRAD) prefetch_row(tb.state + elem, rowf, li, Lg);
+    }
+    const uint32_t n = s1 - s0 < (uint32_t)kPrefetchRows ? s1 - s0 : (uint32_t)kPrefetchRows;
+    for (uint32_t q = 0; q < n; ++q)
+        prefetch_row(a.grad + (int64_t)(bags[s0 + q] - tB) * a.ld + tb.doff, rowf, li, Lg);
+}
+
+__global__ void __launch_bounds__(kThreads, 3) reduce_update_chunks(ReduceArgs a)
+{
+    extern __shared__ uint32_t smem_runs[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t chunk = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     if (chunk >= a.nchunks) return;
-    const int64_t p0 = chunk * a.chunk;
-    const int64_t p1 = p0 + a.chunk < a.n ? p0 + a.chunk : a.n;
+    // per warp: run starts [2c+2], run keys [2c+2], bag of every lookup [2c]
+    const int cap = 2 * (int)a.chunk + 2;
+    uint32_t* runs = smem_runs + (size_t)warp * (3 * cap);
+    uint32_t* rkeys = runs + cap;
+    uint32_t* bags = rkeys + cap;
     const uint32_t limit = a.key_limit_dev ? (uint32_t)*a.key_limit_dev : a.key_limit;
-    const bool has_before = p0 > 0;
-    const uint32_t key_before = has_before ? a.skeys[p0 - 1] : 0u;
-    const bool has_after = p1 < a.n;
-    const uint32_t key_after = has_after ? a.skeys[p1] : 0u;
 
-    RunState r;
-    r.open = false;
-    uint32_t prev_key = key_before;
-    bool prev_valid = has_before;
-    int64_t run_end = p0;
+    const int64_t p0 = chunk_start(a, chunk, lane);
+    const int64_t p1 = chunk + 1 < a.nchunks ? chunk_start(a, chunk + 1, lane) : a.n;
+    if (p0 >= p1) return;
+    const bool first_before = p0 > 0 && a.skeys[p0] == a.skeys[p0 - 1];
+    const bool last_after = p1 < a.n && a.skeys[p1] == a.skeys[p1 - 1];
+
+    // 1. stage the chunk's bags and list its runs (offsets from p0); p0 always opens one
+    int R = 0;
     for (int64_t w = p0; w < p1; w += 32) {
-        const int64_t q = w + lane;
-        const bool inb = q < p1;
-        const uint32_t k = inb ? a.skeys[q] : 0xFFFFFFFFu;
-        const uint32_t bg = inb ? a.sbags[q] : 0u;
-        const bool kv = inb && k < limit;
-        const int nv = __popc(__ballot_sync(0xffffffffu, kv));   // valid lookups form a prefix
-        uint32_t kp = __shfl_up_sync(0xffffffffu, k, 1);
-        bool head;
-        if (lane == 0) head = !prev_valid || k != prev_key;
-        else head = k != kp;
-        const uint32_t hmask = __ballot_sync(0xffffffffu, head && kv);
-        int pos = 0;
-        while (pos < nv) {
-            const bool is_head = (hmask >> pos) & 1u;
-            const uint32_t key = __shfl_sync(0xffffffffu, k, pos);
-            if (is_head) {
-                if (r.open) finalize(r, a, chunk, false);
-                open_run(r, a, key, __shfl_sync(0xffffffffu, bg, pos), false, lane);
-            } else if (!r.open) {
-                // continuation of a run that began before this chunk
-                open_run(r, a, key, __shfl_sync(0xffffffffu, bg, pos), true, lane);
-            }
-            const uint32_t later = pos + 1 < 32 ? (hmask & ~((2u << pos) - 1u)) : 0u;
-            const int end = later ? (__ffs(later) - 1) : nv;
-            accumulate(r, a, bg, pos, end);
-            pos = end;
+        const int64_t p = w + lane;
+        bool head = false;
+        uint32_t k = 0;
+        if (p < p1) {
+            k = a.skeys[p];
+            bags[p - p0] = a.sbags[p];
+            head = p == p0 || k != a.skeys[p - 1];
         }
-        run_end = w + nv;
-        prev_key = __shfl_sync(0xffffffffu, k, 31);
-        prev_valid = true;
-        if (nv < 32 && w + nv < p1) break;      // the rest of the chunk is beyond the key limit
+        const uint32_t m = __ballot_sync(0xffffffffu, head);
+        if (head) {
+            const int slot = R + __popc(m & ((1u << lane) - 1u));
+            runs[slot] = (uint32_t)(p - p0);
+            rkeys[slot] = k;
+        }
+        R += __popc(m);
     }
-    if (r.open) {
-        const bool ext = run_end == p1 && has_after && key_after == r.key;
-        finalize(r, a, chunk, ext);
+    if (lane == 0) runs[R] = (uint32_t)(p1 - p0);
+    __syncwarp();
+
+    // 2. lane groups take runs g, g+G, ...; the runs two steps ahead are
+    //    prefetched into L2 while the current one is reduced and applied
+    const int Lg = a.lanes_per_row;
+    const int G = 32 / Lg;
+    const int li = lane & (Lg - 1), g = lane / Lg;
+    const uint32_t gmask = Lg == 32 ? 0xffffffffu : (((1u << Lg) - 1u) << (g * Lg));
+    prefetch_run(a, runs, rkeys, bags, g, R, first_before, last_after, limit, li, Lg);
+    prefetch_run(a, runs, rkeys, bags, g + G, R, first_before, last_after, limit, li, Lg);
+    for (int r = g; r < R; r += G) {
+        prefetch_run(a, runs, rkeys, bags, r + 2 * G, R, first_before, last_after, limit, li, Lg);
+        const uint32_t key = rkeys[r];
+        if (key >= limit) continue;
+        const int s0 = (int)runs[r], s1 = (int)runs[r + 1];
+        const bool before = r == 0 && first_before;
+        const bool after = r == R - 1 && last_after;
+        const int t = (int)(bags[s0] / (uint32_t)a.batch);
+        const TableDev& tb = a.tables[t];
+        const uint32_t tB = (uint32_t)t * (uint32_t)a.batch;
+        const bool mean = tb.pooling == EMB_POOL_MEAN;
+        const bool colok = 4 * li < tb.dim;
+        // a run applied here loads its row now, overlapping the gradient gathers
+        float4 wv = make_float4(0.f, 0.f, 0.f, 0.f), av = wv;
+        int64_t elem = 0;
+        if (!before && !after && colok) {
+            const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
+            elem = (int64_t)(gid - tb.row_base) * tb.dim + 4 * li;
+            wv = load_w4(tb.w, tb.dtype, elem);
+            av = load_state4(tb, elem);
+        }
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+        if (colok) {
+            const float* gcol = a.grad + tb.doff + 4 * li;
+            int q = s0;
+            for (; q + 1 < s1; q += 2) {
+                const uint32_t ba = bags[q], bb = bags[q + 1];
+                const float4 ga = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(ba - tB) * a.ld));
+                const float4 gb = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(bb - tB) * a.ld));
+                float sa = 1.f, sb = 1.f;
+                if (mean) {
+                    sa = __ldg(a.bag_scale + ba);
+                    sb = __ldg(a.bag_scale + bb);
+                }
+                kahan_add(s[0], c[0], mean ? __fmul_rn(ga.x, sa) : ga.x);
+                kahan_add(s[1], c[1], mean ? __fmul_rn(ga.y, sa) : ga.y);
+                kahan_add(s[2], c[2], mean ? __fmul_rn(ga.z, sa) : ga.z);
+                kahan_add(s[3], c[3], mean ? __fmul_rn(ga.w, sa) : ga.w);
+                kahan_add(s[0], c[0], mean ? __fmul_rn(gb.x, sb) : gb.x);
+                kahan_add(s[1], c[1], mean ? __fmul_rn(gb.y, sb) : gb.y);
+                kahan_add(s[2], c[2], mean ? __fmul_rn(gb.z, sb) : gb.z);
+                kahan_add(s[3], c[3], mean ? __fmul_rn(gb.w, sb) : gb.w);
+            }
+            if (q < s1) {
+                const uint32_t ba = bags[q];
+                const float4 ga = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(ba - tB) * a.ld));
+                const float sa = mean ? __ldg(a.bag_scale + ba) : 1.f;
+                kahan_add(s[0], c[0], mean ? __fmul_rn(ga.x, sa) : ga.x);
+                kahan_add(s[1], c[1], mean ? __fmul_rn(ga.y, sa) : ga.y);
+                kahan_add(s[2], c[2], mean ? __fmul_rn(ga.z, sa) : ga.z);
+                kahan_add(s[3], c[3], mean ? __fmul_rn(ga.w, sa) : ga.w);
+            }
+            float gs[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) gs[k] = __fsub_rn(s[k], c[k]);
+            if (before || after) {
+                float* sp = slot_ptr(a.slots, chunk, before ? kSlotHead : kSlotTail);
+                *reinterpret_cast<float4*>(sp + 4 * li) = make_float4(gs[0], gs[1], gs[2], gs[3]);
+            } else {
+                apply_update4(tb, elem, gs, wv, av);
+            }
+        }
+        // the chunk where a split run starts registers it for the combine kernel
+        if (after && !before && li == 0) a.split_list[atomicAdd(a.split_count, 1)] = (uint32_t)chunk;
+        __syncwarp(gmask);
     }
 }
 
@@ -282,7 +301,14 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
     const uint32_t key = a.skeys[pb];
     for (int64_t base = c;; base += kThreads) {
         const int64_t cc = base + threadIdx.x;
-        const bool cont = cc + 1 < a.nchunks && a.skeys[(cc + 1) * a.chunk] == key;
+        // chunk cc+1 starts inside the run iff the whole window of its nominal
+        // start holds this key (otherwise its start snapped to a later run)
+        bool cont = false;
+        if (cc + 1 < a.nchunks) {
+            const int64_t w0 = (cc + 1) * a.chunk;
+            const int64_t w1 = w0 + a.chunk < a.n ? w0 + a.chunk : a.n;
+            cont = a.skeys[w0] == key && a.skeys[w1 - 1] == key;
+        }
         const int cnt = __syncthreads_count(cont);
         if (cnt < kThreads) {
             if (threadIdx.x == 0) s_last = base + cnt;
@@ -347,7 +373,11 @@ int launch_reduce_update(const ReduceArgs& a, cudaStream_t st)
     if (cudaMemsetAsync(a.split_count, 0, sizeof(int), st) != cudaSuccess) return -1;
     const int64_t threads = a.nchunks * 32;
     const unsigned blocks = (unsigned)((threads + kThreads - 1) / kThreads);
-    reduce_update_chunks<<<blocks, kThreads, 0, st>>>(a);
+    const size_t smem = sizeof(uint32_t) * (size_t)(kThreads / 32) * (size_t)(3 * (2 * a.chunk + 2));
+    if (cudaFuncSetAttribute(reduce_update_chunks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return -1;
+    reduce_update_chunks<<<blocks, kThreads, smem, st>>>(a);
     int launched = 1;
     if (a.nchunks > 1) {
         int dev = 0, sms = 152;

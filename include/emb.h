@@ -176,7 +176,7 @@ int emb_unique(const int64_t* keys, int64_t n, int64_t* unique, int32_t* inverse
  * embedding method.
  *
  * Arguments and results are exactly those of emb_unique, minus the workspace:
- * the scratch is one array compiled into the library (about 9 MB of device
+ * the scratch is one array compiled into the library (12 MB of device
  * memory, held on every GPU that loads the library until the process exits).
  * n must be at most EMB_UNIQUE_NOALLOC_MAX_KEYS; larger n returns
  * EMB_ERR_INVALID_ARG and enqueues nothing.  The first call on a device looks

@@ -226,6 +226,8 @@ def main():
     ap.add_argument("--cpu-sample-batch", type=int, default=16384)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--early-dedup", action="store_true",
+                    help="run the dedup inside the forward on the layer's second stream (overlap)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch size (small profiling cases)")
     ap.add_argument("--rows-cap", type=int, default=0, help="cap every table's rows (small profiling cases)")
     args = ap.parse_args()
@@ -271,6 +273,8 @@ def main():
 
     layer = EmbeddingLayer(w.tables, w.batch, max_nnz)
     layer.init_uniform(w.seed, w.w_lo, w.w_hi)
+    if args.early_dedup:
+        layer.set_early_dedup(args.variant)
 
     def step(i):
         k = i % args.batches
@@ -433,6 +437,8 @@ def main():
                        " [rows capped at %d]" % args.rows_cap if args.rows_cap else ""),
                    "batch": w.batch, "nnz": nnz,
                    "unique_rows": int(U_t.sum()), "variant": args.variant, "batches_cycled": args.batches,
+                   "dedup": "overlapped with the forward on the layer's second stream" if args.early_dedup
+                            else "inside the backward",
                    "l2": "inputs larger than L2 (tables %.1f GB; out, grad_out %.0f MB each)" % (
                        sum(s.rows * s.dim * (_wbytes(s.dtype) + (4 if s.opt == "adagrad" else 0))
                            for s in w.tables) / 1e9, w.batch * w.total_dim * 4 / 1e6),

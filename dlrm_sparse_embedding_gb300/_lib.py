@@ -30,7 +30,7 @@ EXPORTS = (
     "emb_create", "emb_destroy", "emb_init_uniform", "emb_forward", "emb_backward_update",
     "emb_set_keep_dedup", "emb_dedup_result", "emb_unique_workspace", "emb_unique",
     "emb_get_rows", "emb_set_rows", "emb_gather_rows", "emb_sync_status", "emb_launch_count",
-    "emb_set_timing", "emb_phase_times", "emb_unique_noalloc", "emb_status_string",
+    "emb_set_timing", "emb_phase_times", "emb_unique_noalloc", "emb_set_early_dedup", "emb_status_string",
 )
 UNIQUE_NOALLOC_MAX_KEYS = 262144
 PHASES = ("forward", "dedup", "reduce_update")
@@ -67,6 +67,7 @@ def _load() -> ctypes.CDLL:
     L.emb_forward.argtypes = [vp, vp, vp, vp, i64, i32, vp, vp]
     L.emb_backward_update.argtypes = [vp, vp, i32, vp]
     L.emb_set_keep_dedup.argtypes = [vp, i32]
+    L.emb_set_early_dedup.argtypes = [vp, i32]
     L.emb_dedup_result.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.POINTER(i64), vp]
     L.emb_unique_workspace.argtypes = [i64, ctypes.POINTER(ctypes.c_size_t)]
     L.emb_unique.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]

@@ -139,10 +139,12 @@ struct FwdArgs {
     float* bag_scale;           // 1/L per mean-pooled bag
     uint32_t sentinel;          // = total rows: sorts after every valid id
     int64_t warps_per_table;
+    bool write_ids;             // the pooling kernel also writes gid_out / bag_out
     int* err;
 };
 
 int launch_forward(const FwdArgs& a, cudaStream_t st);
+int launch_forward_ids(const FwdArgs& a, cudaStream_t st);   // gid_out / bag_out only
 
 // dedup helpers (dedup.cu); each returns kernels launched or -1
 int launch_hash_insert(const uint32_t* gid, int64_t n, uint32_t limit, uint32_t* table, uint32_t mask,

@@ -134,8 +134,10 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_pool(FwdArgs a)
         const bool valid = in && my_tid_ok && key >= 0 && key < tb.rows;
         if (valid) prefetch_row_l2(tb, key);
         if (in) {
-            a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
-            a.bag_out[i] = (uint32_t)(j0 + li);
+            if (a.write_ids) {
+                a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
+                a.bag_out[i] = (uint32_t)(j0 + li);
+            }
             if (!valid && my_tid_ok) atomicOr(a.err, ERRBIT_KEY_RANGE);
         }
         for (int q = 0; q < nbg; q += kPrefetch) {
@@ -176,8 +178,10 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_pool(FwdArgs a)
         const bool tok = __shfl_sync(gmask, my_tid_ok, k, Lr);
         const bool valid = in && tok && key >= 0 && key < tb.rows;
         if (in) {
-            a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
-            a.bag_out[i] = (uint32_t)(j0 + k);
+            if (a.write_ids) {
+                a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
+                a.bag_out[i] = (uint32_t)(j0 + k);
+            }
             if (!valid && tok) atomicOr(a.err, ERRBIT_KEY_RANGE);
         }
         const int cnt = (int)((K1 - base) < Lr ? (K1 - base) : Lr);
@@ -207,7 +211,57 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_pool(FwdArgs a)
 #undef CLOSE_BAGS
 }
 
+// Global row id and bag of every lookup, nothing else: the forward's id
+// output on its own, so the dedup can start while the pooling kernel runs.
+// A warp owns 32 consecutive bags of one table and streams their keys.
+__global__ void __launch_bounds__(kThreads) fwd_ids(FwdArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const int t = (int)(gw / a.warps_per_table);
+    if (t >= a.num_tables) return;
+    const int64_t B = a.batch;
+    const int64_t bg0 = (gw - (int64_t)t * a.warps_per_table) * 32;
+    const int nbg = (int)(B - bg0 < 32 ? B - bg0 : 32);
+    const int64_t j0 = (int64_t)t * B + bg0;
+    const int64_t rows = a.tables[t].rows;
+    const uint32_t row_base = a.tables[t].row_base;
+    const int64_t K0 = __ldg(a.offsets + j0);
+    int64_t my_end = INT64_MAX;
+    bool my_tid_ok = true;
+    if (lane < nbg) {
+        my_end = __ldg(a.offsets + j0 + lane + 1);
+        my_tid_ok = __ldg(a.table_ids + j0 + lane) == t;
+    }
+    const int64_t K1 = __shfl_sync(0xffffffffu, my_end, nbg - 1);
+    for (int64_t base = K0; base < K1; base += 32) {
+        const int64_t i = base + lane;
+        int k = 0;
+#pragma unroll
+        for (int stp = 16; stp > 0; stp >>= 1) {
+            const int64_t e = __shfl_sync(0xffffffffu, my_end, k + stp - 1);
+            if (e <= i) k += stp;
+        }
+        const bool tok = __shfl_sync(0xffffffffu, my_tid_ok, k);
+        if (i < K1) {
+            const int64_t key = __ldg(a.keys + i);
+            const bool valid = tok && key >= 0 && key < rows;
+            a.gid_out[i] = valid ? row_base + (uint32_t)key : a.sentinel;
+            a.bag_out[i] = (uint32_t)(j0 + k);
+        }
+    }
+}
+
 }  // namespace
+
+int launch_forward_ids(const FwdArgs& a, cudaStream_t st)
+{
+    const int64_t warps = a.warps_per_table * a.num_tables;
+    if (warps <= 0) return 0;
+    const unsigned blocks = (unsigned)((warps * 32 + kThreads - 1) / kThreads);
+    fwd_ids<<<blocks, kThreads, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
 
 int launch_forward(const FwdArgs& a, cudaStream_t st)
 {

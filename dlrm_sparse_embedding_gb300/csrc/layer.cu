@@ -68,10 +68,18 @@ struct emb_layer {
     const uint32_t* last_sorted_bags = nullptr;
     int64_t launches = 0;
 
-    // phase timing (events recorded on the caller's stream)
+    // dedup run inside emb_forward on an internal stream (-1: off)
+    int32_t early_variant = -1;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_in = nullptr, ev_ready = nullptr;
+    bool early_pending = false;           // a forward started a dedup on `side`
+    int32_t early_pending_variant = -1;
+    ReduceArgs early_r{};                 // where that dedup leaves its sorted keys and bags
+
+    // phase timing: events around the forward kernel, the dedup and the
+    // reduction, recorded on the streams that run them
     bool timing = false;
-    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};   // fwd start/end, bwd start, reduce start
-    cudaEvent_t ev_end = nullptr;                                // bwd end
+    cudaEvent_t ev[6] = {};               // fwd start/end, dedup start/end, reduce start/end
     bool fwd_pending = false, bwd_pending = false;
     double phase_ms[EMB_NUM_PHASES] = {0, 0, 0};
     int64_t timed_steps = 0;
@@ -261,9 +269,9 @@ void harvest_timing(emb_layer* L)
         L->fwd_pending = false;
     }
     if (L->bwd_pending) {
-        if (cudaEventSynchronize(L->ev_end) == cudaSuccess) {
+        if (cudaEventSynchronize(L->ev[5]) == cudaSuccess) {
             if (cudaEventElapsedTime(&ms, L->ev[2], L->ev[3]) == cudaSuccess) L->phase_ms[EMB_PHASE_DEDUP] += ms;
-            if (cudaEventElapsedTime(&ms, L->ev[3], L->ev_end) == cudaSuccess)
+            if (cudaEventElapsedTime(&ms, L->ev[4], L->ev[5]) == cudaSuccess)
                 L->phase_ms[EMB_PHASE_REDUCE_UPDATE] += ms;
         }
         L->bwd_pending = false;
@@ -403,7 +411,9 @@ int emb_destroy(emb_layer* L)
     cudaDeviceSynchronize();
     for (cudaEvent_t& e : L->ev)
         if (e) cudaEventDestroy(e);
-    if (L->ev_end) cudaEventDestroy(L->ev_end);
+    if (L->ev_in) cudaEventDestroy(L->ev_in);
+    if (L->ev_ready) cudaEventDestroy(L->ev_ready);
+    if (L->side) cudaStreamDestroy(L->side);
     free_all(L);
     delete L;
     return EMB_OK;
@@ -422,93 +432,16 @@ int emb_init_uniform(emb_layer* L, uint64_t seed, float lo, float hi, void* stre
     return cudaGetLastError() == cudaSuccess ? EMB_OK : EMB_ERR_CUDA;
 }
 
-int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const int32_t* table_ids, int64_t nnz,
-                int32_t batch, float* out, void* stream)
+// Launches the dedup of `variant` over the ids in L->gid / L->bag on st and
+// points r at its sorted keys and bags (plus the unique-index mapping for the
+// hash variant).  Records the by-product pointers for emb_dedup_result.
+static int launch_dedup(emb_layer* L, int32_t variant, int64_t n, cudaStream_t st, ReduceArgs& r)
 {
-    if (!L || !offsets || !table_ids || !out || batch < 1 || batch > L->max_batch || nnz < 0 || nnz > L->max_nnz ||
-        (nnz > 0 && !keys) || !aligned16(out))
-        return EMB_ERR_INVALID_ARG;
-    FwdArgs a;
-    a.keys = keys;
-    a.offsets = offsets;
-    a.table_ids = table_ids;
-    a.batch = batch;
-    a.num_tables = L->T;
-    a.out = out;
-    a.ld = L->total_dim;
-    a.tables = L->d_tables;
-    a.gid_out = L->gid;
-    a.bag_out = L->bag;
-    a.bag_scale = L->bag_scale;
-    a.sentinel = (uint32_t)L->total_rows;
-    a.warps_per_table = (batch + 31) / 32;
-    a.err = L->err;
-    if (L->timing) {
-        harvest_timing(L);
-        cudaEventRecord(L->ev[0], S(stream));
-    }
-    int rc = track(L, launch_forward(a, S(stream)));
-    if (L->timing && rc == EMB_OK) {
-        cudaEventRecord(L->ev[1], S(stream));
-        L->fwd_pending = true;
-    }
-    if (rc != EMB_OK) return rc;
-    L->fwd_done = true;
-    L->last_nnz = nnz;
-    L->last_batch = batch;
-    L->dedup_valid = false;
-    return EMB_OK;
-}
-
-int emb_set_keep_dedup(emb_layer* L, int32_t keep)
-{
-    if (!L) return EMB_ERR_INVALID_ARG;
-    L->keep_dedup = keep != 0;
-    return EMB_OK;
-}
-
-int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, void* stream)
-{
-    if (!L || !grad_out || !aligned16(grad_out) || variant < 0 || variant > 2) return EMB_ERR_INVALID_ARG;
-    if (!L->fwd_done) return EMB_ERR_STATE;
-    cudaStream_t st = S(stream);
-    const int64_t n = L->last_nnz;
     const uint32_t limit = (uint32_t)L->total_rows;
-    ReduceArgs r{};
-    r.n = n;
-    r.chunk = chunk_for(n);
-    r.nchunks = (n + r.chunk - 1) / r.chunk;
+    int rc = EMB_OK;
     r.key_limit = limit;
     r.key_limit_dev = nullptr;
-    {
-        int lg = 1;
-        while (lg < 32 && 4 * lg < L->maxdim) lg <<= 1;
-        r.lanes_per_row = lg;
-    }
     r.gid_of_key = nullptr;
-    r.tables = L->d_tables;
-    r.num_tables = L->T;
-    r.batch = L->last_batch;
-    r.grad = grad_out;
-    r.ld = L->total_dim;
-    r.bag_scale = L->bag_scale;
-    r.slots = L->slots;
-    r.split_list = L->split_list;
-    r.split_count = L->split_count;
-    r.err = L->err;
-    int rc = EMB_OK;
-    L->dedup_valid = false;
-    if (L->timing) cudaEventRecord(L->ev[2], st);
-    if (n == 0) {
-        if (cudaMemsetAsync(L->num_unique, 0, sizeof(int64_t), st) != cudaSuccess ||
-            cudaMemsetAsync(L->seg_off, 0, sizeof(int32_t), st) != cudaSuccess)
-            return EMB_ERR_CUDA;
-        L->dedup_valid = true;
-        L->dedup_variant = variant;
-        L->last_unique32 = L->uniq32;
-        L->last_sorted_bags = L->sv;
-        return EMB_OK;
-    }
     if (variant == EMB_BWD_REDUCTION) {
         rc = track(L, radix_sort_pairs<uint32_t>(L->plan_gid, L->gid, L->bag, L->sk, L->sv, L->tk, L->tv, L->sort_desc,
                                                  L->sort_aux, n, nullptr, nullptr, nullptr, L->err, st));
@@ -555,12 +488,145 @@ int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, vo
         L->last_unique32 = L->ukey_s;
         L->last_sorted_bags = L->sv;
     }
-    if (L->timing) cudaEventRecord(L->ev[3], st);
+    return rc;
+}
+
+int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const int32_t* table_ids, int64_t nnz,
+                int32_t batch, float* out, void* stream)
+{
+    if (!L || !offsets || !table_ids || !out || batch < 1 || batch > L->max_batch || nnz < 0 || nnz > L->max_nnz ||
+        (nnz > 0 && !keys) || !aligned16(out))
+        return EMB_ERR_INVALID_ARG;
+    cudaStream_t st = S(stream);
+    FwdArgs a;
+    a.keys = keys;
+    a.offsets = offsets;
+    a.table_ids = table_ids;
+    a.batch = batch;
+    a.num_tables = L->T;
+    a.out = out;
+    a.ld = L->total_dim;
+    a.tables = L->d_tables;
+    a.gid_out = L->gid;
+    a.bag_out = L->bag;
+    a.bag_scale = L->bag_scale;
+    a.sentinel = (uint32_t)L->total_rows;
+    a.warps_per_table = (batch + 31) / 32;
+    a.write_ids = true;
+    a.err = L->err;
+    if (L->timing) harvest_timing(L);
+    int rc = EMB_OK;
+    const bool early = L->early_variant >= 0 && nnz > 0;
+    if (early) {
+        // ids + dedup on the side stream, concurrent with the pooling kernel
+        a.write_ids = false;
+        if (cudaEventRecord(L->ev_in, st) != cudaSuccess || cudaStreamWaitEvent(L->side, L->ev_in, 0) != cudaSuccess)
+            return EMB_ERR_CUDA;
+        if (L->timing) cudaEventRecord(L->ev[2], L->side);
+        rc = track(L, launch_forward_ids(a, L->side));
+        L->early_r = ReduceArgs{};
+        if (rc == EMB_OK) rc = launch_dedup(L, L->early_variant, nnz, L->side, L->early_r);
+        if (L->timing) cudaEventRecord(L->ev[3], L->side);
+        if (rc == EMB_OK && cudaEventRecord(L->ev_ready, L->side) != cudaSuccess) rc = EMB_ERR_CUDA;
+        if (rc != EMB_OK) return rc;
+    }
+    if (L->timing) cudaEventRecord(L->ev[0], st);
+    rc = track(L, launch_forward(a, st));
+    if (L->timing && rc == EMB_OK) {
+        cudaEventRecord(L->ev[1], st);
+        L->fwd_pending = true;
+    }
+    if (rc != EMB_OK) return rc;
+    L->fwd_done = true;
+    L->last_nnz = nnz;
+    L->last_batch = batch;
+    L->dedup_valid = false;
+    L->early_pending = early;
+    L->early_pending_variant = early ? L->early_variant : -1;
+    return EMB_OK;
+}
+
+int emb_set_keep_dedup(emb_layer* L, int32_t keep)
+{
+    if (!L) return EMB_ERR_INVALID_ARG;
+    L->keep_dedup = keep != 0;
+    return EMB_OK;
+}
+
+int emb_set_early_dedup(emb_layer* L, int32_t variant)
+{
+    if (!L || variant < -1 || variant > 2) return EMB_ERR_INVALID_ARG;
+    if (variant >= 0 && !L->side) {
+        if (cudaStreamCreateWithFlags(&L->side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&L->ev_in, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&L->ev_ready, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            return EMB_ERR_CUDA;
+        }
+    }
+    L->early_variant = variant;
+    return EMB_OK;
+}
+
+int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, void* stream)
+{
+    if (!L || !grad_out || !aligned16(grad_out) || variant < 0 || variant > 2) return EMB_ERR_INVALID_ARG;
+    if (!L->fwd_done) return EMB_ERR_STATE;
+    cudaStream_t st = S(stream);
+    const int64_t n = L->last_nnz;
+    ReduceArgs r{};
+    r.n = n;
+    r.chunk = chunk_for(n);
+    r.nchunks = (n + r.chunk - 1) / r.chunk;
+    {
+        int lg = 1;
+        while (lg < 32 && 4 * lg < L->maxdim) lg <<= 1;
+        r.lanes_per_row = lg;
+    }
+    r.tables = L->d_tables;
+    r.num_tables = L->T;
+    r.batch = L->last_batch;
+    r.grad = grad_out;
+    r.ld = L->total_dim;
+    r.bag_scale = L->bag_scale;
+    r.slots = L->slots;
+    r.split_list = L->split_list;
+    r.split_count = L->split_count;
+    r.err = L->err;
+    int rc = EMB_OK;
+    L->dedup_valid = false;
+    if (n == 0) {
+        if (cudaMemsetAsync(L->num_unique, 0, sizeof(int64_t), st) != cudaSuccess ||
+            cudaMemsetAsync(L->seg_off, 0, sizeof(int32_t), st) != cudaSuccess)
+            return EMB_ERR_CUDA;
+        L->dedup_valid = true;
+        L->dedup_variant = variant;
+        L->last_unique32 = L->uniq32;
+        L->last_sorted_bags = L->sv;
+        return EMB_OK;
+    }
+    if (L->early_pending) {
+        // the ids (and maybe the dedup) were produced on the side stream
+        if (cudaStreamWaitEvent(st, L->ev_ready, 0) != cudaSuccess) return EMB_ERR_CUDA;
+    }
+    if (L->early_pending && L->early_pending_variant == variant) {
+        r.skeys = L->early_r.skeys;
+        r.sbags = L->early_r.sbags;
+        r.key_limit = L->early_r.key_limit;
+        r.key_limit_dev = L->early_r.key_limit_dev;
+        r.gid_of_key = L->early_r.gid_of_key;
+    } else {
+        if (L->timing) cudaEventRecord(L->ev[2], st);
+        rc = launch_dedup(L, variant, n, st, r);
+        if (L->timing) cudaEventRecord(L->ev[3], st);
+    }
+    L->early_pending = false;
+    if (L->timing) cudaEventRecord(L->ev[4], st);
     if (rc == EMB_OK) rc = track(L, launch_reduce_update(r, st));
     if (rc == EMB_OK && variant == EMB_BWD_UNIQUE_HASH)
         rc = track(L, launch_hash_clear(L->htable, L->uslot_s, L->num_unique, n, st));
     if (L->timing && rc == EMB_OK) {
-        cudaEventRecord(L->ev_end, st);
+        cudaEventRecord(L->ev[5], st);
         L->bwd_pending = true;
     }
     if (rc != EMB_OK) return rc;
@@ -710,7 +776,6 @@ int emb_set_timing(emb_layer* L, int32_t enable)
     if (enable && !L->ev[0]) {
         for (cudaEvent_t& e : L->ev)
             if (cudaEventCreate(&e) != cudaSuccess) return EMB_ERR_CUDA;
-        if (cudaEventCreate(&L->ev_end) != cudaSuccess) return EMB_ERR_CUDA;
     }
     if (!enable) harvest_timing(L);
     L->timing = enable != 0;

@@ -106,6 +106,11 @@ class EmbeddingLayer:
     def set_keep_dedup(self, keep: bool) -> None:
         check(lib.emb_set_keep_dedup(self._h, 1 if keep else 0))
 
+    def set_early_dedup(self, variant: Optional[str]) -> None:
+        """Run the given backward variant's dedup inside forward(), on the
+        layer's own stream, overlapping the pooling kernel (None: off)."""
+        check(lib.emb_set_early_dedup(self._h, -1 if variant is None else VARIANTS[variant]), "emb_set_early_dedup")
+
     def dedup_result(self, with_inverse: bool = True, stream=None):
         """(unique int64[U], inverse int32[nnz] or None, counts int32[U],
         seg_offsets int32[U+1], sorted_bags int32[nnz]) of the last backward."""

@@ -131,6 +131,18 @@ int emb_forward(emb_layer* layer, const int64_t* keys, const int64_t* offsets,
  * EMB_ERR_STATE if no forward preceded it. */
 int emb_backward_update(emb_layer* layer, const float* grad_out, int32_t variant, void* stream);
 
+/* Early dedup.  With variant >= 0 (an emb_bwd_variant), every later
+ * emb_forward also enqueues the dedup of that backward variant on an
+ * internal stream of the layer: the global ids and bags are extracted and
+ * sorted (or hashed) while the pooling kernel runs on the caller's stream --
+ * the dedup needs only the batch's keys, not the pooled output.  A following
+ * emb_backward_update on the caller's stream waits for it and, if called with
+ * the same variant, goes straight to the segmented reduction (with another
+ * variant it redoes the dedup).  Results are identical to the default mode.
+ * variant = -1 (default) turns it off.  The caller's input buffers must stay
+ * valid until that backward is enqueued; no extra memory is used. */
+int emb_set_early_dedup(emb_layer* layer, int32_t variant);
+
 /* Keep (1) or drop (0, default) the dedup by-products of later backwards so
  * emb_dedup_result can return them.  EMB_BWD_REDUCTION then also writes the
  * sorted unique ids, counts and segment offsets it otherwise never forms. */
@@ -218,7 +230,8 @@ int emb_launch_count(emb_layer* layer, int64_t* count_host, int32_t reset);
  * fused lookup/pooling kernel), EMB_PHASE_DEDUP (global-id sort or hash
  * dedup, from the start of emb_backward_update up to the reduction) and
  * EMB_PHASE_REDUCE_UPDATE (segmented reduction + optimizer kernels) -- and
- * adds their elapsed times.  emb_phase_times waits for the last recorded
+ * adds their elapsed times.  With early dedup the dedup phase runs on the
+ * layer's internal stream, overlapping the forward.  emb_phase_times waits for the last recorded
  * events, writes the accumulated milliseconds of the n (<= 3) phases and the
  * number of steps they cover, and, with reset = 1, clears them. */
 enum { EMB_PHASE_FORWARD = 0, EMB_PHASE_DEDUP = 1, EMB_PHASE_REDUCE_UPDATE = 2, EMB_NUM_PHASES = 3 };

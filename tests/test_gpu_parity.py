@@ -311,3 +311,35 @@ def test_allocation_failure_returns_oom_and_leaks_nothing():
     assert r.stdout.startswith("OOM"), r.stdout
     leaked = int(r.stdout.split()[1])
     assert leaked < (64 << 20)
+
+
+@pytest.mark.parametrize("early,bwd", [("reduction", "reduction"), ("unique_sort", "unique_sort"),
+                                       ("unique_hash", "unique_hash"), ("reduction", "unique_hash"),
+                                       ("unique_hash", "reduction")])
+def test_early_dedup_is_bitwise_identical(early, bwd):
+    import torch
+    from dlrm_sparse_embedding_gb300 import EMB_OK, EmbeddingLayer
+    w = _small("skew_small").replace(batch=700)
+    batch = ci.make_batch(w)
+    grad = torch.from_numpy(ci.make_grad(w)).cuda()
+    keys, offs, tids = (torch.from_numpy(x).cuda() for x in (batch.keys, batch.offsets, batch.table_ids))
+    res = []
+    for mode in (None, early):
+        layer = EmbeddingLayer(w.tables, w.batch, batch.nnz)
+        try:
+            layer.init_uniform(3, w.w_lo, w.w_hi)
+            layer.set_early_dedup(mode)
+            layer.set_keep_dedup(True)
+            outs = []
+            for _ in range(2):                      # two steps: the second reuses the side stream
+                outs.append(layer.forward(keys, offs, tids, w.batch).cpu().numpy())
+                layer.backward_update(grad, bwd)
+            assert layer.sync_status() == EMB_OK
+            ded = [x.cpu().numpy() for x in layer.dedup_result(with_inverse=False) if x is not None]
+            rows = [layer.get_rows(t, 0, 512)[0] for t in range(w.num_tables)]
+            res.append((outs, ded, rows))
+        finally:
+            layer.close()
+    (o0, d0, r0), (o1, d1, r1) = res
+    for a, b in zip(o0 + d0 + r0, o1 + d1 + r1):
+        assert np.array_equal(a, b)

@@ -87,7 +87,7 @@ struct emb_layer {
 
 namespace {
 
-constexpr int64_t kTargetChunks = 32768;
+constexpr int64_t kTargetChunks = 65536;
 constexpr int64_t kMinChunk = 32, kMaxChunk = 256;
 
 // Nominal lookups per warp in the segmented reduction: enough chunks to fill

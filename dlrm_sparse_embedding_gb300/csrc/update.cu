@@ -17,11 +17,9 @@
 // lookups, so only runs longer than a chunk are ever cut.  The warp lists the
 // runs of its chunk in shared memory together with the bag of every lookup;
 // lane groups of Lg = next_pow2(dim/4) lanes (one float4 column each) take
-// runs round-robin, so dims below 128 have several runs in flight per warp,
-// and every group asks L2 for the rows of the runs two steps ahead (table row,
-// accumulator, first gradient rows) while it reduces the current one.  A run
-// inside the chunk is reduced and applied by its group; its table row and
-// accumulator are loaded when the run starts, overlapping the gradient
+// runs round-robin, so dims below 128 have several runs in flight per warp.
+// A run inside the chunk is reduced and applied by its group; its table row
+// and accumulator are loaded when the run starts, overlapping the gradient
 // gathers.  A run that crosses chunk boundaries is cut into
 // pieces; each chunk writes its piece's partial sum into a per-chunk slot, the
 // chunk where the run starts registers it in a compact list, and a second
@@ -133,48 +131,6 @@ __device__ __forceinline__ int64_t chunk_start(const ReduceArgs& a, int64_t c, i
     return base;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
-// Asks L2 for every 128-byte line of `bytes` bytes at p, spread over the
-// group's lanes (rows are at most 512 bytes: at most 4 lines).
-__device__ __forceinline__ void prefetch_row(const void* p, int bytes, int li, int Lg)
-{
-    const char* c = static_cast<const char*>(p);
-    for (int off = li * 128; off < bytes; off += Lg * 128) prefetch_l2(c + off);
-}
-
-constexpr int kPrefetchRows = 8;   // gradient rows of a future run asked for ahead of time
-
-// Issues L2 prefetches for run r (its table row, accumulator and first
-// gradient rows) so they are on chip when the group reaches it.
-__device__ __forceinline__ void prefetch_run(const ReduceArgs& a, const uint32_t* runs, const uint32_t* rkeys,
-                                             const uint32_t* bags, int r, int R, bool first_before, bool last_after,
-                                             uint32_t limit, int li, int Lg)
-{
-    if (r >= R) return;
-    const uint32_t key = rkeys[r];
-    if (key >= limit) return;
-    const uint32_t s0 = runs[r], s1 = runs[r + 1];
-    const uint32_t bag0 = bags[s0];
-    const int t = (int)(bag0 / (uint32_t)a.batch);
-    const TableDev& tb = a.tables[t];
-    const int rowf = tb.dim * 4;
-    const uint32_t tB = (uint32_t)t * (uint32_t)a.batch;
-    if (!(r == 0 && first_before) && !(r == R - 1 && last_after)) {
-        const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
-        const int64_t elem = (int64_t)(gid - tb.row_base) * tb.dim;
-        const int wb = tb.dtype == EMB_F32 ? 4 : 2;
-        prefetch_row(static_cast<const char*>(tb.w) + elem * wb, tb.dim * wb, li, Lg);
-        if (tb.opt == EMB_OPT_ADAGRAD) prefetch_row(tb.state + elem, rowf, li, Lg);
-    }
-    const uint32_t n = s1 - s0 < (uint32_t)kPrefetchRows ? s1 - s0 : (uint32_t)kPrefetchRows;
-    for (uint32_t q = 0; q < n; ++q)
-        prefetch_row(a.grad + (int64_t)(bags[s0 + q] - tB) * a.ld + tb.doff, rowf, li, Lg);
-}
-
 __global__ void __launch_bounds__(kThreads, 3) reduce_update_chunks(ReduceArgs a)
 {
     extern __shared__ uint32_t smem_runs[];
@@ -216,16 +172,12 @@ __global__ void __launch_bounds__(kThreads, 3) reduce_update_chunks(ReduceArgs a
     if (lane == 0) runs[R] = (uint32_t)(p1 - p0);
     __syncwarp();
 
-    // 2. lane groups take runs g, g+G, ...; the runs two steps ahead are
-    //    prefetched into L2 while the current one is reduced and applied
+    // 2. lane groups take runs g, g+G, ...: reduce each and apply it
     const int Lg = a.lanes_per_row;
     const int G = 32 / Lg;
     const int li = lane & (Lg - 1), g = lane / Lg;
     const uint32_t gmask = Lg == 32 ? 0xffffffffu : (((1u << Lg) - 1u) << (g * Lg));
-    prefetch_run(a, runs, rkeys, bags, g, R, first_before, last_after, limit, li, Lg);
-    prefetch_run(a, runs, rkeys, bags, g + G, R, first_before, last_after, limit, li, Lg);
     for (int r = g; r < R; r += G) {
-        prefetch_run(a, runs, rkeys, bags, r + 2 * G, R, first_before, last_after, limit, li, Lg);
         const uint32_t key = rkeys[r];
         if (key >= limit) continue;
         const int s0 = (int)runs[r], s1 = (int)runs[r + 1];

@@ -45,7 +45,7 @@ struct TableDev {
 // radix sort of (key, u32 value) pairs
 // ---------------------------------------------------------------------------
 constexpr int kSortThreads = 256;
-constexpr int kSortItemsSmall = 4;      // 1024-element tiles for n <= kSmallSortMax
+constexpr int kSortItemsSmall = 8;      // 2048-element tiles for n <= kSmallSortMax
 constexpr int kSortItemsLarge = 8;      // 2048-element tiles above
 constexpr int64_t kSmallSortMax = int64_t(8) << 20;
 constexpr int kMaxDigitBits = 10;
@@ -107,7 +107,6 @@ struct ReduceArgs {
     int64_t n;
     int64_t chunk;              // nominal positions per warp (starts snap to run starts)
     int64_t nchunks;
-    int32_t lanes_per_row;      // Lg: lanes sharing one row, one float4 column each (power of two, 4*Lg >= max dim)
     uint32_t key_limit;         // keys >= limit are skipped ...
     const int64_t* key_limit_dev; // ... or >= *key_limit_dev when non-null
     const uint32_t* gid_of_key; // null: key is the global id

@@ -578,11 +578,6 @@ int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, vo
     r.n = n;
     r.chunk = chunk_for(n);
     r.nchunks = (n + r.chunk - 1) / r.chunk;
-    {
-        int lg = 1;
-        while (lg < 32 && 4 * lg < L->maxdim) lg <<= 1;
-        r.lanes_per_row = lg;
-    }
     r.tables = L->d_tables;
     r.num_tables = L->T;
     r.batch = L->last_batch;

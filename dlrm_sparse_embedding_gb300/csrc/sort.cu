@@ -4,7 +4,7 @@
 // de recomendacion a escala", section "Integracion del cluster": RB reduces
 // over equal keys, UB dedups the keys first).
 //
-// Small inputs (up to 8 Mi keys) run three kernels per pass over 1024-key
+// Small inputs (up to 8 Mi keys) run three kernels per pass over 2048-key
 // tiles: per-tile digit histogram, a scan of each digit's row over tiles, and
 // stable in-tile ranking in shared memory with coalesced runs written to
 // bucket start + tile offset.  Large inputs run one histogram kernel (the
@@ -630,7 +630,7 @@ static int sort_passes(const SortPlan& plan, const K* keys_in, const uint32_t* v
 
 // Small inputs (at most kSmallSortMax keys, where a look-back would walk long
 // chains of concurrently running tiles) take the three-kernel pass over
-// 1024-key tiles; large ones the one-kernel pass over 2048-key tiles.
+// 2048-key tiles; large ones the one-kernel pass over 2048-key tiles.
 template <typename K>
 int radix_sort_pairs(const SortPlan& plan, const K* keys_in, const uint32_t* vals_in, K* keys_out,
                      uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp, uint64_t* desc, uint32_t* aux,

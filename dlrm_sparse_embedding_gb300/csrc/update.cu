@@ -16,17 +16,20 @@
 // each chunk boundary snaps forward to the next run start within `chunk`
 // lookups, so only runs longer than a chunk are ever cut.  The warp lists the
 // runs of its chunk in shared memory together with the bag of every lookup;
-// lane groups of Lg = next_pow2(dim/4) lanes (one float4 column each) take
-// runs round-robin, so dims below 128 have several runs in flight per warp.
-// A run inside the chunk is reduced and applied by its group; its table row
-// and accumulator are loaded when the run starts, overlapping the gradient
-// gathers.  A run that crosses chunk boundaries is cut into
-// pieces; each chunk writes its piece's partial sum into a per-chunk slot, the
+// lane groups of Lg = next_pow2(dim/4) lanes (one float4 column each, dim the
+// widest table in the chunk) take runs round-robin, so dims below 128 have
+// several runs in flight per warp; a chunk that holds a single run (a piece
+// of a hot row) has all groups share its lookups instead.  A run inside the
+// chunk is reduced and applied by its group; its table row and accumulator
+// are loaded when the run starts, overlapping the gradient gathers.  A run
+// that crosses chunk boundaries is cut into pieces; each chunk writes its
+// piece's partial sum into a per-chunk slot, the
 // chunk where the run starts registers it in a compact list, and a second
 // kernel (persistent blocks over that list) adds the pieces in chunk order and
 // applies the update.  Every sum is a compensated (Kahan) fp32 sum in a fixed
-// order, so results are deterministic and independent of scheduling; there are
-// no atomics on values.
+// order (gradient rows are added in pairs before each compensated step), so
+// results are deterministic and independent of scheduling; there are no
+// atomics on values.
 #include "emb_internal.cuh"
 
 namespace emb {
@@ -131,7 +134,7 @@ __device__ __forceinline__ int64_t chunk_start(const ReduceArgs& a, int64_t c, i
     return base;
 }
 
-__global__ void __launch_bounds__(kThreads, 3) reduce_update_chunks(ReduceArgs a)
+__global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a)
 {
     extern __shared__ uint32_t smem_runs[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -172,11 +175,84 @@ __global__ void __launch_bounds__(kThreads, 3) reduce_update_chunks(ReduceArgs a
     if (lane == 0) runs[R] = (uint32_t)(p1 - p0);
     __syncwarp();
 
-    // 2. lane groups take runs g, g+G, ...: reduce each and apply it
-    const int Lg = a.lanes_per_row;
+    // lanes per row for this chunk: enough for the widest table among its runs
+    // (the chunk's lookups are sorted, so its tables form one range, usually one table)
+    int Lg = 1;
+    {
+        const int t_first = (int)(bags[0] / (uint32_t)a.batch);
+        const int t_last = (int)(bags[p1 - p0 - 1] / (uint32_t)a.batch);
+        int maxdim = 4;
+        for (int t = t_first; t <= t_last; ++t) maxdim = max(maxdim, a.tables[t].dim);
+        while (4 * Lg < maxdim) Lg <<= 1;
+    }
+
     const int G = 32 / Lg;
     const int li = lane & (Lg - 1), g = lane / Lg;
     const uint32_t gmask = Lg == 32 ? 0xffffffffu : (((1u << Lg) - 1u) << (g * Lg));
+
+    if (R == 1 && G > 1) {
+        // 2a. the chunk is one run, usually a piece of a hot row: all lane
+        //     groups share its lookups, then their sums are merged
+        const uint32_t key = rkeys[0];
+        if (key >= limit) return;
+        const int np = (int)(p1 - p0);
+        const bool before = first_before, after = last_after;
+        const int t = (int)(bags[0] / (uint32_t)a.batch);
+        const TableDev& tb = a.tables[t];
+        const uint32_t tB = (uint32_t)t * (uint32_t)a.batch;
+        const bool mean = tb.pooling == EMB_POOL_MEAN;
+        const bool colok = 4 * li < tb.dim;
+        float4 wv = make_float4(0.f, 0.f, 0.f, 0.f), av = wv;
+        int64_t elem = 0;
+        if (!before && !after && colok && g == 0) {
+            const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
+            elem = (int64_t)(gid - tb.row_base) * tb.dim + 4 * li;
+            wv = load_w4(tb.w, tb.dtype, elem);
+            av = load_state4(tb, elem);
+        }
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+        if (colok) {
+            const float* gcol = a.grad + tb.doff + 4 * li;
+            for (int q = g; q < np; q += 2 * G) {
+                const bool hb = q + G < np;
+                const uint32_t ba = bags[q], bb = hb ? bags[q + G] : ba;
+                const float4 ga = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(ba - tB) * a.ld));
+                float4 gb = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (hb) gb = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(bb - tB) * a.ld));
+                const float sa = mean ? __ldg(a.bag_scale + ba) : 1.f;
+                const float sb = (mean && hb) ? __ldg(a.bag_scale + bb) : 1.f;
+                kahan_add(s[0], c[0], __fadd_rn(mean ? __fmul_rn(ga.x, sa) : ga.x, mean ? __fmul_rn(gb.x, sb) : gb.x));
+                kahan_add(s[1], c[1], __fadd_rn(mean ? __fmul_rn(ga.y, sa) : ga.y, mean ? __fmul_rn(gb.y, sb) : gb.y));
+                kahan_add(s[2], c[2], __fadd_rn(mean ? __fmul_rn(ga.z, sa) : ga.z, mean ? __fmul_rn(gb.z, sb) : gb.z));
+                kahan_add(s[3], c[3], __fadd_rn(mean ? __fmul_rn(ga.w, sa) : ga.w, mean ? __fmul_rn(gb.w, sb) : gb.w));
+            }
+        }
+        // merge the groups' compensated sums (fixed butterfly order)
+        for (int off = Lg; off < 32; off <<= 1) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float os = __shfl_xor_sync(0xffffffffu, s[k], off);
+                const float oc = __shfl_xor_sync(0xffffffffu, c[k], off);
+                kahan_add(s[k], c[k], os);
+                kahan_add(s[k], c[k], -oc);
+            }
+        }
+        if (g == 0 && colok) {
+            float gs[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) gs[k] = __fsub_rn(s[k], c[k]);
+            if (before || after) {
+                float* sp = slot_ptr(a.slots, chunk, before ? kSlotHead : kSlotTail);
+                *reinterpret_cast<float4*>(sp + 4 * li) = make_float4(gs[0], gs[1], gs[2], gs[3]);
+            } else {
+                apply_update4(tb, elem, gs, wv, av);
+            }
+        }
+        if (after && !before && lane == 0) a.split_list[atomicAdd(a.split_count, 1)] = (uint32_t)chunk;
+        return;
+    }
+
+    // 2b. lane groups take runs g, g+G, ...: reduce each and apply it
     for (int r = g; r < R; r += G) {
         const uint32_t key = rkeys[r];
         if (key >= limit) continue;
@@ -210,14 +286,11 @@ __global__ void __launch_bounds__(kThreads, 3) reduce_update_chunks(ReduceArgs a
                     sa = __ldg(a.bag_scale + ba);
                     sb = __ldg(a.bag_scale + bb);
                 }
-                kahan_add(s[0], c[0], mean ? __fmul_rn(ga.x, sa) : ga.x);
-                kahan_add(s[1], c[1], mean ? __fmul_rn(ga.y, sa) : ga.y);
-                kahan_add(s[2], c[2], mean ? __fmul_rn(ga.z, sa) : ga.z);
-                kahan_add(s[3], c[3], mean ? __fmul_rn(ga.w, sa) : ga.w);
-                kahan_add(s[0], c[0], mean ? __fmul_rn(gb.x, sb) : gb.x);
-                kahan_add(s[1], c[1], mean ? __fmul_rn(gb.y, sb) : gb.y);
-                kahan_add(s[2], c[2], mean ? __fmul_rn(gb.z, sb) : gb.z);
-                kahan_add(s[3], c[3], mean ? __fmul_rn(gb.w, sb) : gb.w);
+                // the pair is added in plain fp32, then compensated into the run sum
+                kahan_add(s[0], c[0], __fadd_rn(mean ? __fmul_rn(ga.x, sa) : ga.x, mean ? __fmul_rn(gb.x, sb) : gb.x));
+                kahan_add(s[1], c[1], __fadd_rn(mean ? __fmul_rn(ga.y, sa) : ga.y, mean ? __fmul_rn(gb.y, sb) : gb.y));
+                kahan_add(s[2], c[2], __fadd_rn(mean ? __fmul_rn(ga.z, sa) : ga.z, mean ? __fmul_rn(gb.z, sb) : gb.z));
+                kahan_add(s[3], c[3], __fadd_rn(mean ? __fmul_rn(ga.w, sa) : ga.w, mean ? __fmul_rn(gb.w, sb) : gb.w));
             }
             if (q < s1) {
                 const uint32_t ba = bags[q];

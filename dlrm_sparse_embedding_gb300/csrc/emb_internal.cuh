@@ -42,6 +42,83 @@ struct TableDev {
 };
 
 // ---------------------------------------------------------------------------
+// device helpers shared by the reduction kernels: compensated (Kahan) fp32
+// addition, row loads/stores in the table dtype (16-byte fp32 or 8-byte 16-bit
+// vectors of 4 columns) and one optimizer step on 4 columns
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x)
+{
+    float y = __fsub_rn(x, c);
+    float t = __fadd_rn(s, y);
+    c = __fsub_rn(__fsub_rn(t, s), y);
+    s = t;
+}
+
+__device__ __forceinline__ float4 load_w4(const void* w, int dtype, int64_t elem)
+{
+    if (dtype == EMB_F32) return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(w) + elem));
+    uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(w) + elem));
+    float4 r;
+    if (dtype == EMB_F16) {
+        __half2 a = *reinterpret_cast<__half2*>(&raw.x), b = *reinterpret_cast<__half2*>(&raw.y);
+        float2 fa = __half22float2(a), fb = __half22float2(b);
+        r = make_float4(fa.x, fa.y, fb.x, fb.y);
+    } else {
+        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&raw.x), b = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
+        float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+        r = make_float4(fa.x, fa.y, fb.x, fb.y);
+    }
+    return r;
+}
+
+__device__ __forceinline__ void store_w4(void* w, int dtype, int64_t elem, float4 v)
+{
+    if (dtype == EMB_F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(w) + elem) = v;
+        return;
+    }
+    uint2 raw;
+    if (dtype == EMB_F16) {
+        __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        raw.x = *reinterpret_cast<uint32_t*>(&a);
+        raw.y = *reinterpret_cast<uint32_t*>(&b);
+    } else {
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        raw.x = *reinterpret_cast<uint32_t*>(&a);
+        raw.y = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint2*>(static_cast<unsigned short*>(w) + elem) = raw;
+}
+
+// One optimizer step on 4 consecutive elements of a row whose current values
+// (w, and a for Adagrad) have already been loaded.
+__device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t elem, const float g[4], float4 w, float4 a)
+{
+    float wv[4] = {w.x, w.y, w.z, w.w};
+    if (tb.opt == EMB_OPT_ADAGRAD) {
+        float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            av[q] = __fmaf_rn(g[q], g[q], av[q]);
+            float den = __fadd_rn(__fsqrt_rn(av[q]), tb.eps);
+            wv[q] = __fmaf_rn(-tb.lr, __fdiv_rn(g[q], den), wv[q]);
+        }
+        *reinterpret_cast<float4*>(tb.state + elem) = make_float4(av[0], av[1], av[2], av[3]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) wv[q] = __fmaf_rn(-tb.lr, g[q], wv[q]);
+    }
+    store_w4(tb.w, tb.dtype, elem, make_float4(wv[0], wv[1], wv[2], wv[3]));
+}
+
+
+__device__ __forceinline__ float4 load_state4(const TableDev& tb, int64_t elem)
+{
+    if (tb.opt != EMB_OPT_ADAGRAD) return make_float4(0.f, 0.f, 0.f, 0.f);
+    return *reinterpret_cast<const float4*>(tb.state + elem);
+}
+
+// ---------------------------------------------------------------------------
 // radix sort of (key, u32 value) pairs
 // ---------------------------------------------------------------------------
 constexpr int kSortThreads = 256;

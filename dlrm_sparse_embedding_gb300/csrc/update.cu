@@ -38,71 +38,6 @@ namespace {
 
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ void kahan_add(float& s, float& c, float x)
-{
-    float y = __fsub_rn(x, c);
-    float t = __fadd_rn(s, y);
-    c = __fsub_rn(__fsub_rn(t, s), y);
-    s = t;
-}
-
-__device__ __forceinline__ float4 load_w4(const void* w, int dtype, int64_t elem)
-{
-    if (dtype == EMB_F32) return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(w) + elem));
-    uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const unsigned short*>(w) + elem));
-    float4 r;
-    if (dtype == EMB_F16) {
-        __half2 a = *reinterpret_cast<__half2*>(&raw.x), b = *reinterpret_cast<__half2*>(&raw.y);
-        float2 fa = __half22float2(a), fb = __half22float2(b);
-        r = make_float4(fa.x, fa.y, fb.x, fb.y);
-    } else {
-        __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&raw.x), b = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
-        float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
-        r = make_float4(fa.x, fa.y, fb.x, fb.y);
-    }
-    return r;
-}
-
-__device__ __forceinline__ void store_w4(void* w, int dtype, int64_t elem, float4 v)
-{
-    if (dtype == EMB_F32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(w) + elem) = v;
-        return;
-    }
-    uint2 raw;
-    if (dtype == EMB_F16) {
-        __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
-        raw.x = *reinterpret_cast<uint32_t*>(&a);
-        raw.y = *reinterpret_cast<uint32_t*>(&b);
-    } else {
-        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
-        raw.x = *reinterpret_cast<uint32_t*>(&a);
-        raw.y = *reinterpret_cast<uint32_t*>(&b);
-    }
-    *reinterpret_cast<uint2*>(static_cast<unsigned short*>(w) + elem) = raw;
-}
-
-// One optimizer step on 4 consecutive elements of a row whose current values
-// (w, and a for Adagrad) have already been loaded.
-__device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t elem, const float g[4], float4 w, float4 a)
-{
-    float wv[4] = {w.x, w.y, w.z, w.w};
-    if (tb.opt == EMB_OPT_ADAGRAD) {
-        float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            av[q] = __fmaf_rn(g[q], g[q], av[q]);
-            float den = __fadd_rn(__fsqrt_rn(av[q]), tb.eps);
-            wv[q] = __fmaf_rn(-tb.lr, __fdiv_rn(g[q], den), wv[q]);
-        }
-        *reinterpret_cast<float4*>(tb.state + elem) = make_float4(av[0], av[1], av[2], av[3]);
-    } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) wv[q] = __fmaf_rn(-tb.lr, g[q], wv[q]);
-    }
-    store_w4(tb.w, tb.dtype, elem, make_float4(wv[0], wv[1], wv[2], wv[3]));
-}
-
 __device__ __forceinline__ float* slot_ptr(float* slots, int64_t chunk, int which)
 {
     return slots + ((chunk * 2 + which) * kMaxDim);
@@ -110,11 +45,6 @@ __device__ __forceinline__ float* slot_ptr(float* slots, int64_t chunk, int whic
 
 enum { kSlotHead = 0, kSlotTail = 1 };
 
-__device__ __forceinline__ float4 load_state4(const TableDev& tb, int64_t elem)
-{
-    if (tb.opt != EMB_OPT_ADAGRAD) return make_float4(0.f, 0.f, 0.f, 0.f);
-    return *reinterpret_cast<const float4*>(tb.state + elem);
-}
 
 // Snapped chunk start: the first run start in [c*chunk, c*chunk + chunk), or
 // c*chunk itself when a run covers that whole window.  Whole warp.
@@ -134,17 +64,34 @@ __device__ __forceinline__ int64_t chunk_start(const ReduceArgs& a, int64_t c, i
     return base;
 }
 
+// Shared memory per warp, in 32-bit words: run starts [2c+2] (entry
+// indices), entry bags [2c+2], entry start offsets [2c+1] (u16), padded to 16 B.
+__host__ __device__ __forceinline__ int64_t warp_words(int64_t c) { return (5 * c + 5 + 3) & ~int64_t(3); }
+
+// Gradient term of one entry: f * grad_out[b, col..col+3], f = multiplicity
+// (times 1/L_b for mean pooling).
+__device__ __forceinline__ float4 entry_term(const float* gcol, int64_t ld, uint32_t b, uint32_t tB, float f)
+{
+    const float4 g = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(b - tB) * ld));
+    return make_float4(__fmul_rn(g.x, f), __fmul_rn(g.y, f), __fmul_rn(g.z, f), __fmul_rn(g.w, f));
+}
+
+__device__ __forceinline__ float entry_factor(const ReduceArgs& a, const uint16_t* epos, int e, uint32_t b, bool mean)
+{
+    const float f = (float)(epos[e + 1] - epos[e]);
+    return mean ? __fmul_rn(f, __ldg(a.bag_scale + b)) : f;
+}
+
 __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a)
 {
     extern __shared__ uint32_t smem_runs[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t chunk = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     if (chunk >= a.nchunks) return;
-    // per warp: run starts [2c+2], run keys [2c+2], bag of every lookup [2c]
     const int cap = 2 * (int)a.chunk + 2;
-    uint32_t* runs = smem_runs + (size_t)warp * (3 * cap);
-    uint32_t* rkeys = runs + cap;
-    uint32_t* bags = rkeys + cap;
+    uint32_t* runs = smem_runs + (size_t)warp * warp_words(a.chunk);
+    uint32_t* ebag = runs + cap;
+    uint16_t* epos = reinterpret_cast<uint16_t*>(ebag + cap);
     const uint32_t limit = a.key_limit_dev ? (uint32_t)*a.key_limit_dev : a.key_limit;
 
     const int64_t p0 = chunk_start(a, chunk, lane);
@@ -153,34 +100,52 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
     const bool first_before = p0 > 0 && a.skeys[p0] == a.skeys[p0 - 1];
     const bool last_after = p1 < a.n && a.skeys[p1] == a.skeys[p1 - 1];
 
-    // 1. stage the chunk's bags and list its runs (offsets from p0); p0 always opens one
-    int R = 0;
+    // 1. stage the chunk as entries -- maximal groups of equal (key, bag); a
+    //    run lists its lookups in bag order, so a bag that hits a row several
+    //    times forms one entry -- and list the runs as entry ranges.  Entry e
+    //    covers offsets [epos[e], epos[e+1]) from p0; p0 always opens a run.
+    int R = 0, E = 0;
+    uint32_t prev_k = 0, prev_b = 0;
     for (int64_t w = p0; w < p1; w += 32) {
         const int64_t p = w + lane;
-        bool head = false;
-        uint32_t k = 0;
-        if (p < p1) {
+        const bool valid = p < p1;
+        uint32_t k = 0, b = 0;
+        if (valid) {
             k = a.skeys[p];
-            bags[p - p0] = a.sbags[p];
-            head = p == p0 || k != a.skeys[p - 1];
+            b = a.sbags[p];
         }
-        const uint32_t m = __ballot_sync(0xffffffffu, head);
-        if (head) {
-            const int slot = R + __popc(m & ((1u << lane) - 1u));
-            runs[slot] = (uint32_t)(p - p0);
-            rkeys[slot] = k;
+        uint32_t pk = __shfl_up_sync(0xffffffffu, k, 1), pb = __shfl_up_sync(0xffffffffu, b, 1);
+        if (lane == 0) {
+            pk = prev_k;
+            pb = prev_b;
         }
-        R += __popc(m);
+        const bool khead = valid && (p == p0 || k != pk);
+        const bool bhead = valid && (khead || b != pb);
+        const uint32_t km = __ballot_sync(0xffffffffu, khead), bm = __ballot_sync(0xffffffffu, bhead);
+        const uint32_t below = (1u << lane) - 1u;
+        const int e = E + __popc(bm & below);
+        if (bhead) {
+            ebag[e] = b;
+            epos[e] = (uint16_t)(p - p0);
+        }
+        if (khead) runs[R + __popc(km & below)] = (uint32_t)e;
+        E += __popc(bm);
+        R += __popc(km);
+        prev_k = __shfl_sync(0xffffffffu, k, 31);
+        prev_b = __shfl_sync(0xffffffffu, b, 31);
     }
-    if (lane == 0) runs[R] = (uint32_t)(p1 - p0);
+    if (lane == 0) {
+        runs[R] = (uint32_t)E;
+        epos[E] = (uint16_t)(p1 - p0);
+    }
     __syncwarp();
 
     // lanes per row for this chunk: enough for the widest table among its runs
     // (the chunk's lookups are sorted, so its tables form one range, usually one table)
     int Lg = 1;
     {
-        const int t_first = (int)(bags[0] / (uint32_t)a.batch);
-        const int t_last = (int)(bags[p1 - p0 - 1] / (uint32_t)a.batch);
+        const int t_first = (int)(ebag[0] / (uint32_t)a.batch);
+        const int t_last = (int)(ebag[E - 1] / (uint32_t)a.batch);
         int maxdim = 4;
         for (int t = t_first; t <= t_last; ++t) maxdim = max(maxdim, a.tables[t].dim);
         while (4 * Lg < maxdim) Lg <<= 1;
@@ -192,12 +157,11 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
 
     if (R == 1 && G > 1) {
         // 2a. the chunk is one run, usually a piece of a hot row: all lane
-        //     groups share its lookups, then their sums are merged
-        const uint32_t key = rkeys[0];
+        //     groups share its entries, then their sums are merged
+        const uint32_t key = a.skeys[p0];
         if (key >= limit) return;
-        const int np = (int)(p1 - p0);
         const bool before = first_before, after = last_after;
-        const int t = (int)(bags[0] / (uint32_t)a.batch);
+        const int t = (int)(ebag[0] / (uint32_t)a.batch);
         const TableDev& tb = a.tables[t];
         const uint32_t tB = (uint32_t)t * (uint32_t)a.batch;
         const bool mean = tb.pooling == EMB_POOL_MEAN;
@@ -213,18 +177,16 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
         float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
         if (colok) {
             const float* gcol = a.grad + tb.doff + 4 * li;
-            for (int q = g; q < np; q += 2 * G) {
-                const bool hb = q + G < np;
-                const uint32_t ba = bags[q], bb = hb ? bags[q + G] : ba;
-                const float4 ga = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(ba - tB) * a.ld));
-                float4 gb = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (hb) gb = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(bb - tB) * a.ld));
-                const float sa = mean ? __ldg(a.bag_scale + ba) : 1.f;
-                const float sb = (mean && hb) ? __ldg(a.bag_scale + bb) : 1.f;
-                kahan_add(s[0], c[0], __fadd_rn(mean ? __fmul_rn(ga.x, sa) : ga.x, mean ? __fmul_rn(gb.x, sb) : gb.x));
-                kahan_add(s[1], c[1], __fadd_rn(mean ? __fmul_rn(ga.y, sa) : ga.y, mean ? __fmul_rn(gb.y, sb) : gb.y));
-                kahan_add(s[2], c[2], __fadd_rn(mean ? __fmul_rn(ga.z, sa) : ga.z, mean ? __fmul_rn(gb.z, sb) : gb.z));
-                kahan_add(s[3], c[3], __fadd_rn(mean ? __fmul_rn(ga.w, sa) : ga.w, mean ? __fmul_rn(gb.w, sb) : gb.w));
+            for (int q = g; q < E; q += 2 * G) {
+                const bool hb = q + G < E;
+                const uint32_t ba = ebag[q], bb = hb ? ebag[q + G] : ba;
+                const float4 ta = entry_term(gcol, a.ld, ba, tB, entry_factor(a, epos, q, ba, mean));
+                float4 tb4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (hb) tb4 = entry_term(gcol, a.ld, bb, tB, entry_factor(a, epos, q + G, bb, mean));
+                kahan_add(s[0], c[0], __fadd_rn(ta.x, tb4.x));
+                kahan_add(s[1], c[1], __fadd_rn(ta.y, tb4.y));
+                kahan_add(s[2], c[2], __fadd_rn(ta.z, tb4.z));
+                kahan_add(s[3], c[3], __fadd_rn(ta.w, tb4.w));
             }
         }
         // merge the groups' compensated sums (fixed butterfly order)
@@ -254,12 +216,12 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
 
     // 2b. lane groups take runs g, g+G, ...: reduce each and apply it
     for (int r = g; r < R; r += G) {
-        const uint32_t key = rkeys[r];
+        const int e0 = (int)runs[r], e1 = (int)runs[r + 1];
+        const uint32_t key = a.skeys[p0 + epos[e0]];
         if (key >= limit) continue;
-        const int s0 = (int)runs[r], s1 = (int)runs[r + 1];
         const bool before = r == 0 && first_before;
         const bool after = r == R - 1 && last_after;
-        const int t = (int)(bags[s0] / (uint32_t)a.batch);
+        const int t = (int)(ebag[e0] / (uint32_t)a.batch);
         const TableDev& tb = a.tables[t];
         const uint32_t tB = (uint32_t)t * (uint32_t)a.batch;
         const bool mean = tb.pooling == EMB_POOL_MEAN;
@@ -276,30 +238,24 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
         float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
         if (colok) {
             const float* gcol = a.grad + tb.doff + 4 * li;
-            int q = s0;
-            for (; q + 1 < s1; q += 2) {
-                const uint32_t ba = bags[q], bb = bags[q + 1];
-                const float4 ga = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(ba - tB) * a.ld));
-                const float4 gb = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(bb - tB) * a.ld));
-                float sa = 1.f, sb = 1.f;
-                if (mean) {
-                    sa = __ldg(a.bag_scale + ba);
-                    sb = __ldg(a.bag_scale + bb);
-                }
+            int q = e0;
+            for (; q + 1 < e1; q += 2) {
+                const uint32_t ba = ebag[q], bb = ebag[q + 1];
+                const float4 ta = entry_term(gcol, a.ld, ba, tB, entry_factor(a, epos, q, ba, mean));
+                const float4 tb4 = entry_term(gcol, a.ld, bb, tB, entry_factor(a, epos, q + 1, bb, mean));
                 // the pair is added in plain fp32, then compensated into the run sum
-                kahan_add(s[0], c[0], __fadd_rn(mean ? __fmul_rn(ga.x, sa) : ga.x, mean ? __fmul_rn(gb.x, sb) : gb.x));
-                kahan_add(s[1], c[1], __fadd_rn(mean ? __fmul_rn(ga.y, sa) : ga.y, mean ? __fmul_rn(gb.y, sb) : gb.y));
-                kahan_add(s[2], c[2], __fadd_rn(mean ? __fmul_rn(ga.z, sa) : ga.z, mean ? __fmul_rn(gb.z, sb) : gb.z));
-                kahan_add(s[3], c[3], __fadd_rn(mean ? __fmul_rn(ga.w, sa) : ga.w, mean ? __fmul_rn(gb.w, sb) : gb.w));
+                kahan_add(s[0], c[0], __fadd_rn(ta.x, tb4.x));
+                kahan_add(s[1], c[1], __fadd_rn(ta.y, tb4.y));
+                kahan_add(s[2], c[2], __fadd_rn(ta.z, tb4.z));
+                kahan_add(s[3], c[3], __fadd_rn(ta.w, tb4.w));
             }
-            if (q < s1) {
-                const uint32_t ba = bags[q];
-                const float4 ga = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(ba - tB) * a.ld));
-                const float sa = mean ? __ldg(a.bag_scale + ba) : 1.f;
-                kahan_add(s[0], c[0], mean ? __fmul_rn(ga.x, sa) : ga.x);
-                kahan_add(s[1], c[1], mean ? __fmul_rn(ga.y, sa) : ga.y);
-                kahan_add(s[2], c[2], mean ? __fmul_rn(ga.z, sa) : ga.z);
-                kahan_add(s[3], c[3], mean ? __fmul_rn(ga.w, sa) : ga.w);
+            if (q < e1) {
+                const uint32_t ba = ebag[q];
+                const float4 ta = entry_term(gcol, a.ld, ba, tB, entry_factor(a, epos, q, ba, mean));
+                kahan_add(s[0], c[0], ta.x);
+                kahan_add(s[1], c[1], ta.y);
+                kahan_add(s[2], c[2], ta.z);
+                kahan_add(s[3], c[3], ta.w);
             }
             float gs[4];
 #pragma unroll
@@ -398,7 +354,7 @@ int launch_reduce_update(const ReduceArgs& a, cudaStream_t st)
     if (cudaMemsetAsync(a.split_count, 0, sizeof(int), st) != cudaSuccess) return -1;
     const int64_t threads = a.nchunks * 32;
     const unsigned blocks = (unsigned)((threads + kThreads - 1) / kThreads);
-    const size_t smem = sizeof(uint32_t) * (size_t)(kThreads / 32) * (size_t)(3 * (2 * a.chunk + 2));
+    const size_t smem = sizeof(uint32_t) * (size_t)(kThreads / 32) * (size_t)warp_words(a.chunk);
     if (cudaFuncSetAttribute(reduce_update_chunks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return -1;

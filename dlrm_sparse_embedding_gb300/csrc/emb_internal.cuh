@@ -216,6 +216,7 @@ struct FwdArgs {
     uint32_t sentinel;          // = total rows: sorts after every valid id
     int64_t warps_per_table;
     bool write_ids;             // the pooling kernel also writes gid_out / bag_out
+    bool rows16;                // every table stores 16-bit rows (selects the pooling kernel's occupancy)
     int* err;
 };
 

@@ -64,6 +64,16 @@ struct BagStream {
     int64_t cur_end;    // its end offset
 };
 
+__device__ __forceinline__ void kahan_add4(BagStream& st, float4 x)
+{
+    kahan_add(st.s.x, st.c.x, x.x);
+    kahan_add(st.s.y, st.c.y, x.y);
+    kahan_add(st.s.z, st.c.z, x.z);
+    kahan_add(st.s.w, st.c.w, x.w);
+}
+
+constexpr uint32_t kNoRow = 0xFFFFFFFFu;
+
 // Closes (scales and stores) every bag that ends at position `pos`, empty bags included.
 __device__ __forceinline__ void close_bags(BagStream& st, int64_t pos, int nbg, uint32_t gmask, int Lr, int my_len,
                                            int64_t my_end, bool mean, bool colok, float* out_col, int64_t bg0,
@@ -86,7 +96,11 @@ __device__ __forceinline__ void close_bags(BagStream& st, int64_t pos, int nbg, 
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) fwd_pool(FwdArgs a)
+// kMinBlocks: resident blocks per SM the register budget is sized for.  With
+// 16-bit rows a lane holds half the row data in flight, and 4 blocks (64
+// registers) measure faster; fp32 rows take 3 (80 registers).
+template <int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
 {
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
@@ -100,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_pool(FwdArgs a)
     const uint32_t gmask = Lr == 32 ? 0xffffffffu : (((1u << Lr) - 1u) << (g * Lr));
     const bool colok = 4 * li < tb.dim;
     const bool mean = tb.pooling == EMB_POOL_MEAN;
+    const uint32_t lowmask = Lr == 32 ? 0xffffffffu : ((1u << Lr) - 1u);
 
     // this group owns bags bg0 .. bg0+nbg-1 of table t; lane li describes bag li
     const int64_t bg0 = (gw - (int64_t)t * a.warps_per_table) * 32 + (int64_t)g * Lr;
@@ -176,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_pool(FwdArgs a)
             if (e <= i) k += stp;
         }
         const bool tok = __shfl_sync(gmask, my_tid_ok, k, Lr);
+        const int64_t kend = __shfl_sync(gmask, my_end, k, Lr);
         const bool valid = in && tok && key >= 0 && key < tb.rows;
         if (in) {
             if (a.write_ids) {
@@ -184,25 +200,33 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_pool(FwdArgs a)
             }
             if (!valid && tok) atomicOr(a.err, ERRBIT_KEY_RANGE);
         }
+        // bit u: a bag ends right after position base + u
+        const uint32_t endbits = (__ballot_sync(gmask, in && kend == i + 1) >> (g * Lr)) & lowmask;
+        // rows < 2^32 per table, so a key travels as 32 bits; kNoRow = skipped
+        const uint32_t kk = valid ? (uint32_t)key : kNoRow;
         const int cnt = (int)((K1 - base) < Lr ? (K1 - base) : Lr);
         for (int q = 0; q < cnt; q += kPrefetch) {
             float4 v[kPrefetch];
 #pragma unroll
             for (int u = 0; u < kPrefetch; ++u) {
-                const int qq = q + u;
-                const int64_t kq = __shfl_sync(gmask, key, qq & (Lr - 1), Lr);
-                const bool vq = __shfl_sync(gmask, valid, qq & (Lr - 1), Lr) && qq < cnt;
+                const uint32_t kq = __shfl_sync(gmask, kk, (q + u) & (Lr - 1), Lr);
                 v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (vq && colok) v[u] = load_row4(tb.w, tb.dtype, kq * tb.dim + 4 * li);
+                if (kq != kNoRow && q + u < cnt && colok) v[u] = load_row4(tb.w, tb.dtype, (int64_t)kq * tb.dim + 4 * li);
             }
+            // rows are added in pairs, then compensated into the bag's sum; a
+            // bag ending inside a pair takes the first row alone
 #pragma unroll
-            for (int u = 0; u < kPrefetch; ++u) {
+            for (int u = 0; u < kPrefetch; u += 2) {
                 if (q + u < cnt) {
-                    kahan_add(st.s.x, st.c.x, v[u].x);
-                    kahan_add(st.s.y, st.c.y, v[u].y);
-                    kahan_add(st.s.z, st.c.z, v[u].z);
-                    kahan_add(st.s.w, st.c.w, v[u].w);
-                    CLOSE_BAGS(base + q + u + 1);
+                    const bool split = (endbits >> (q + u)) & 1u;
+                    const float4 w1 = split ? make_float4(0.f, 0.f, 0.f, 0.f) : v[u + 1];
+                    kahan_add4(st, make_float4(__fadd_rn(v[u].x, w1.x), __fadd_rn(v[u].y, w1.y),
+                                               __fadd_rn(v[u].z, w1.z), __fadd_rn(v[u].w, w1.w)));
+                    if (split) {
+                        CLOSE_BAGS(base + q + u + 1);
+                        if (q + u + 1 < cnt) kahan_add4(st, v[u + 1]);
+                    }
+                    if ((endbits >> (q + u + 1)) & 1u) CLOSE_BAGS(base + q + u + 2);
                 }
             }
         }
@@ -268,7 +292,10 @@ int launch_forward(const FwdArgs& a, cudaStream_t st)
     const int64_t warps = a.warps_per_table * a.num_tables;
     if (warps <= 0) return 0;
     const unsigned blocks = (unsigned)((warps * 32 + kThreads - 1) / kThreads);
-    fwd_pool<<<blocks, kThreads, 0, st>>>(a);
+    if (a.rows16)
+        fwd_pool<4><<<blocks, kThreads, 0, st>>>(a);
+    else
+        fwd_pool<3><<<blocks, kThreads, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

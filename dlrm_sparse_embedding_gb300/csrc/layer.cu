@@ -513,6 +513,8 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
     a.sentinel = (uint32_t)L->total_rows;
     a.warps_per_table = (batch + 31) / 32;
     a.write_ids = true;
+    a.rows16 = true;
+    for (const TableDev& d : L->tabs) a.rows16 = a.rows16 && d.dtype != EMB_F32;
     a.err = L->err;
     if (L->timing) harvest_timing(L);
     int rc = EMB_OK;

@@ -330,9 +330,18 @@ sort_histogram(const K* __restrict__ keys, int64_t n_host, const int64_t* n_dev,
     for (int i = threadIdx.x; i < np * nb; i += kSortThreads) sh[i] = 0;
     __syncthreads();
     const K sub = key_sub ? (K)(*key_sub) : (K)0;
-    for (int64_t i = (int64_t)blockIdx.x * kSortThreads + threadIdx.x; i < c.n; i += (int64_t)gridDim.x * kSortThreads) {
-        const K k = (K)(keys[i] - sub);
-        for (int p = 0; p < np; ++p) atomicAdd(&sh[p * nb + (int)((k >> (p * D)) & (K)(nb - 1))], 1u);
+    // four independent coalesced loads per thread and round
+    constexpr int kU = 4;
+    const int64_t stride = (int64_t)gridDim.x * kSortThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kSortThreads + threadIdx.x; i < c.n; i += kU * stride) {
+        K k[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) k[u] = i + u * stride < c.n ? (K)(keys[i + u * stride] - sub) : (K)0;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (i + u * stride < c.n)
+                for (int p = 0; p < np; ++p) atomicAdd(&sh[p * nb + (int)((k[u] >> (p * D)) & (K)(nb - 1))], 1u);
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < np * nb; i += kSortThreads)

@@ -37,6 +37,8 @@ namespace emb {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kCombineThreads = 256;
+constexpr int kCombineBlocksPerSM = 4;
 
 __device__ __forceinline__ float* slot_ptr(float* slots, int64_t chunk, int which)
 {
@@ -274,13 +276,16 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
 }
 
 // Adds the pieces of the split run that crosses boundary c (c*chunk), which
-// starts in chunk c-1, and applies its update.  Whole block.
+// starts in chunk c-1, and applies its update.  Whole block: warp w adds
+// pieces w, w+W, w+2W, ... (four loads in flight), then warp 0 adds the warps'
+// sums in warp order.
 __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int64_t& s_last,
                                             float (*part)[kMaxDim])
 {
+    constexpr int W = kCombineThreads / 32;
     const int64_t pb = c * a.chunk;
     const uint32_t key = a.skeys[pb];
-    for (int64_t base = c;; base += kThreads) {
+    for (int64_t base = c;; base += kCombineThreads) {
         const int64_t cc = base + threadIdx.x;
         // chunk cc+1 starts inside the run iff the whole window of its nominal
         // start holds this key (otherwise its start snapped to a later run)
@@ -291,7 +296,7 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
             cont = a.skeys[w0] == key && a.skeys[w1 - 1] == key;
         }
         const int cnt = __syncthreads_count(cont);
-        if (cnt < kThreads) {
+        if (cnt < kCombineThreads) {
             if (threadIdx.x == 0) s_last = base + cnt;
             break;
         }
@@ -306,9 +311,26 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
     const bool colok = 4 * lane < tb.dim;
     float s[4] = {0.f, 0.f, 0.f, 0.f}, cc4[4] = {0.f, 0.f, 0.f, 0.f};
     if (colok) {
-        for (int64_t qi = warp; qi < P; qi += kThreads / 32) {
+        int64_t qi = warp;
+        for (; qi + 3 * W < P; qi += 4 * W) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t q = qi + u * W;
+                const float* sp = q == 0 ? slot_ptr(a.slots, c - 1, kSlotTail) : slot_ptr(a.slots, c - 1 + q, kSlotHead);
+                v[u] = *reinterpret_cast<const float4*>(sp + 4 * lane);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                kahan_add(s[0], cc4[0], v[u].x);
+                kahan_add(s[1], cc4[1], v[u].y);
+                kahan_add(s[2], cc4[2], v[u].z);
+                kahan_add(s[3], cc4[3], v[u].w);
+            }
+        }
+        for (; qi < P; qi += W) {
             const float* sp = qi == 0 ? slot_ptr(a.slots, c - 1, kSlotTail) : slot_ptr(a.slots, c - 1 + qi, kSlotHead);
-            float4 v = *reinterpret_cast<const float4*>(sp + 4 * lane);
+            const float4 v = *reinterpret_cast<const float4*>(sp + 4 * lane);
             kahan_add(s[0], cc4[0], v.x);
             kahan_add(s[1], cc4[1], v.y);
             kahan_add(s[2], cc4[2], v.z);
@@ -320,7 +342,7 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
     __syncthreads();
     if (warp == 0 && colok) {
         float gs[4] = {0.f, 0.f, 0.f, 0.f}, gc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int w = 0; w < kThreads / 32; ++w) {
+        for (int w = 0; w < W; ++w) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) kahan_add(gs[q], gc[q], part[w][4 * lane + q]);
         }
@@ -336,10 +358,10 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
 
 // Persistent blocks over the runs registered as split: each adds its run's
 // pieces in chunk order and applies the update.
-__global__ void __launch_bounds__(kThreads) reduce_update_combine(ReduceArgs a)
+__global__ void __launch_bounds__(kCombineThreads) reduce_update_combine(ReduceArgs a)
 {
     __shared__ int64_t s_last;
-    __shared__ float part[kThreads / 32][kMaxDim];
+    __shared__ float part[kCombineThreads / 32][kMaxDim];
     const int nsplit = *a.split_count;
     for (int item = blockIdx.x; item < nsplit; item += gridDim.x) {
         combine_run(a, (int64_t)a.split_list[item] + 1, s_last, part);
@@ -364,8 +386,9 @@ int launch_reduce_update(const ReduceArgs& a, cudaStream_t st)
         int dev = 0, sms = 152;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        const int64_t grid = (a.nchunks - 1) < 4 * (int64_t)sms ? (a.nchunks - 1) : 4 * (int64_t)sms;
-        reduce_update_combine<<<(unsigned)grid, kThreads, 0, st>>>(a);
+        const int64_t cap = (int64_t)kCombineBlocksPerSM * sms;
+        const int64_t grid = (a.nchunks - 1) < cap ? (a.nchunks - 1) : cap;
+        reduce_update_combine<<<(unsigned)grid, kCombineThreads, 0, st>>>(a);
         ++launched;
     }
     if (cudaGetLastError() != cudaSuccess) return -1;

@@ -122,7 +122,7 @@ __device__ __forceinline__ float4 load_state4(const TableDev& tb, int64_t elem)
 // radix sort of (key, u32 value) pairs
 // ---------------------------------------------------------------------------
 constexpr int kSortThreads = 256;
-constexpr int kSortItemsSmall = 8;      // 2048-element tiles for n <= kSmallSortMax
+constexpr int kSortItemsSmall = 12;     // 3072-element tiles for n <= kSmallSortMax
 constexpr int kSortItemsLarge = 8;      // 2048-element tiles above
 constexpr int64_t kSmallSortMax = int64_t(8) << 20;
 constexpr int kMaxDigitBits = 10;

@@ -95,6 +95,8 @@ __device__ __forceinline__ PassCtx pass_ctx(int64_t n_host, const int64_t* n_dev
 
 // ---- small inputs: three kernels per pass (histogram per tile, scan, ranking) ----
 
+constexpr int kDownsweepBlocks = 4;   // resident blocks per SM the ranking kernel's registers are sized for
+
 template <typename K, int ITEMS>
 __global__ void __launch_bounds__(kSortThreads)
 sort_upsweep(const K* __restrict__ keys_in, const K* keys_out, const K* keys_tmp, int64_t n_host,
@@ -160,7 +162,7 @@ sort_scan(uint32_t* __restrict__ counts, uint32_t* __restrict__ totals, int64_t 
 }
 
 template <typename K, int ITEMS>
-__global__ void __launch_bounds__(kSortThreads)
+__global__ void __launch_bounds__(kSortThreads, kDownsweepBlocks)
 sort_downsweep(const K* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, K* keys_out,
                uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp, int64_t n_host, const int64_t* n_dev,
                const int32_t* bits_dev, int bits_max, int D, int pass, const uint64_t* key_sub,

@@ -49,7 +49,7 @@ class TableSpec:
     dim: int
     dtype: str = "f32"          # storage type: "f32" | "f16" | "bf16"
     pooling: str = "sum"        # "sum" | "mean"
-    opt: str = "sgd"            # "sgd" | "adagrad"
+    opt: str = "sgd"            # "sgd" | "adagrad" | "rowwise_adagrad"
     lr: float = 0.01
     eps: float = 1e-8
     init_acc: float = 0.0

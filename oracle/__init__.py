@@ -9,8 +9,8 @@ ctypes declarations.
 The step it computes, by definition (see the C file for the passages):
   a1 lookup + pooling + concatenation, a2 global row ids, a3 unique keys with
   inverse index, counts and segment offsets, a4 per-unique-row gradient sums,
-  a5 one SGD / Adagrad step per touched row, rounded once into the table's
-  storage type.
+  a5 one SGD / Adagrad / row-wise Adagrad step per touched row, rounded once
+  into the table's storage type.
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_pins.py`` (closed forms, invariants, brute force and
@@ -33,7 +33,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 _DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2}
 _POOL_CODE = {"sum": 0, "mean": 1}
-_OPT_CODE = {"sgd": 0, "adagrad": 1}
+_OPT_CODE = {"sgd": 0, "adagrad": 1, "rowwise_adagrad": 2}
 
 
 def build(force: bool = False) -> str:

@@ -22,7 +22,10 @@
  *  - The optimizers are not on the pages.  SGD is W <- W - lr*G.  Adagrad is
  *    the per-element form of Duchi, Hazan & Singer (JMLR 2011) with eps outside
  *    the square root and the accumulator updated before the weight:
- *    A <- A + G*G ; W <- W - lr*G/(sqrt(A)+eps).
+ *    A <- A + G*G ; W <- W - lr*G/(sqrt(A)+eps).  Row-wise Adagrad keeps one
+ *    accumulator per row and adds the mean over the row's columns of G*G to
+ *    it: A <- A + (1/dim) * sum_c G_c^2 ; W <- W - lr*G/(sqrt(A)+eps) (the
+ *    form used by the open DLRM embedding libraries; the pages do not define it).
  *  - Duplicate keys in one batch: their gradients are summed first and each
  *    touched row gets exactly one optimizer step per batch.
  *
@@ -305,11 +308,15 @@ void ora_reduce_sampled(int32_t T, int32_t B, const int64_t* offsets, const int6
 /* For each row k (table row_table[k], `dim` = dims[row_table[k]]):
  *   SGD:     W' = W - lr*G
  *   Adagrad: A' = A + G*G ;  W' = W - lr*G/(sqrt(A')+eps)
+ *   row-wise Adagrad (opt 2): a' = a + (1/dim) sum_c G_c^2 for the row's one
+ *     accumulator a, W' = W - lr*G/(sqrt(a')+eps); the row store holds a in
+ *     every column of the row (all equal)
  * in binary64 from the stored values; W' is then rounded once to the table
  * storage type (0 fp32, 1 fp16, 2 bf16) and A' to fp32, and both are written
  * back as the binary64 value of the rounded result.  Wscale/Ascale
  * (nullable) receive the magnitude scales |W| + lr*Gabs/(sqrt(A')+eps) (SGD:
- * |W| + lr*Gabs) and A + Gabs^2 used to judge rounding error. */
+ * |W| + lr*Gabs) and A + Gabs^2 (row-wise: a + (1/dim) sum_c Gabs_c^2) used
+ * to judge rounding error. */
 void ora_update(int64_t U, const int32_t* row_table, const int64_t* row_start,
                 const int32_t* dims, const int32_t* dtype, const int32_t* opt,
                 const double* lr, const double* eps,
@@ -319,11 +326,27 @@ void ora_update(int64_t U, const int32_t* row_table, const int64_t* row_start,
     for (int64_t k = 0; k < U; ++k) {
         int32_t t = row_table[k];
         int64_t base = row_start[k];
+        double row_a = 0.0, row_den = 0.0, row_ascale = 0.0;
+        if (opt[t] == 2) {
+            double ssq = 0.0, ssq_abs = 0.0;
+            for (int32_t c = 0; c < dims[t]; ++c) {
+                ssq += G[base + c] * G[base + c];
+                if (Gabs) ssq_abs += Gabs[base + c] * Gabs[base + c];
+            }
+            row_a = A[base] + ssq / (double)dims[t];
+            row_den = sqrt(row_a) + eps[t];
+            row_ascale = A[base] + ssq_abs / (double)dims[t];
+        }
         for (int32_t c = 0; c < dims[t]; ++c) {
             double g = G[base + c];
             double w = W[base + c];
             double wn, step_scale;
-            if (opt[t] == 1) {
+            if (opt[t] == 2) {
+                wn = w - lr[t] * g / row_den;
+                step_scale = Gabs ? lr[t] * Gabs[base + c] / row_den : 0.0;
+                if (Ascale) Ascale[base + c] = row_ascale;
+                A[base + c] = (double)(float)row_a;
+            } else if (opt[t] == 1) {
                 double a = A[base + c] + g * g;
                 double den = sqrt(a) + eps[t];
                 wn = w - lr[t] * g / den;

@@ -379,6 +379,66 @@ def test_adagrad_single_touch_closed_form():
         assert np.array_equal(res.A[s:s + 4], np.float32(g * g).astype(np.float64))
 
 
+def test_rowwise_adagrad_hand_example():
+    # lr 1/2 and eps 0 keep every intermediate exact: row 1 gets G = (3, 4, 0, 0),
+    # mean of squares 25/4, sqrt 5/2, step (3, 4, 0, 0) / 5 = (0.6, 0.8, 0, 0);
+    # row 2 gets G = (2, 2, 2, 2), mean of squares 4, sqrt 2, step 1/2 per column
+    B = 2
+    tables = [_spec(5, 4, "sum", "rowwise_adagrad", lr=0.5, eps=0.0)]
+    keys = np.array([1, 2], dtype=np.int64)
+    offsets = np.arange(B + 1, dtype=np.int64)
+    W0 = np.ones((5, 4), dtype=np.float32)
+    grad = np.array([[3, 4, 0, 0], [2, 2, 2, 2]], dtype=np.float32)
+    res = oracle.step(tables, B, offsets, keys, np.zeros(B, np.int32), grad, _dense_rows([W0]))
+    s1, s2 = res.rows.row_start[0], res.rows.row_start[1]
+    assert res.W[s1:s1 + 4].tolist() == [float(np.float32(0.4)), float(np.float32(0.2)), 1.0, 1.0]
+    assert res.A[s1:s1 + 4].tolist() == [6.25] * 4
+    assert res.W[s2:s2 + 4].tolist() == [0.5] * 4
+    assert res.A[s2:s2 + 4].tolist() == [4.0] * 4
+
+
+def test_rowwise_adagrad_equals_elementwise_when_a_row_has_one_magnitude():
+    # when every column of a row's gradient has the same magnitude and the row
+    # starts from one accumulator value, the mean of squares is that square, so
+    # the row-wise step is the element-wise one (pinned against torch below)
+    B, dim = 12, 8
+    rng = np.random.default_rng(41)
+    keys = np.concatenate([[7, 7, 7, 7], rng.choice(np.arange(8, 30), B - 4, replace=False)]).astype(np.int64)
+    offsets = np.arange(B + 1, dtype=np.int64)
+    W0 = rng.uniform(-0.05, 0.05, (30, dim)).astype(np.float32)
+    signs = rng.choice([-1.0, 1.0], size=(B, dim))
+    # dyadic magnitudes keep the sums of squares exact in binary64
+    grad = (signs * (rng.integers(1, 9, (B, 1)) / 4.0)).astype(np.float32)
+    grad[:4] = np.abs(grad[:4]) * np.sign(grad[0])    # same signs within the row touched four times
+    res = {}
+    for opt in ("adagrad", "rowwise_adagrad"):
+        tables = [_spec(30, dim, "sum", opt, lr=0.01, eps=1e-8)]
+        res[opt] = oracle.step(tables, B, offsets, keys, np.zeros(B, np.int32), grad, _dense_rows([W0]))
+    assert np.array_equal(res["adagrad"].W, res["rowwise_adagrad"].W)
+    assert np.array_equal(res["adagrad"].A, res["rowwise_adagrad"].A)
+
+
+def test_rowwise_adagrad_accumulator_is_one_value_per_row_and_column_order_free():
+    B, dim = 16, 12
+    rng = np.random.default_rng(43)
+    keys = rng.integers(0, 40, B).astype(np.int64)
+    offsets = np.arange(B + 1, dtype=np.int64)
+    W0 = rng.uniform(-0.05, 0.05, (40, dim)).astype(np.float32)
+    grad = rng.standard_normal((B, dim)).astype(np.float32)
+    perm = rng.permutation(dim)
+    tables = [_spec(40, dim, "sum", "rowwise_adagrad")]
+    a = oracle.step(tables, B, offsets, keys, np.zeros(B, np.int32), grad, _dense_rows([W0]))
+    b = oracle.step(tables, B, offsets, keys, np.zeros(B, np.int32), grad[:, perm],
+                    _dense_rows([W0[:, perm]]))
+    for k in range(a.unique.shape[0]):
+        s = a.rows.row_start[k]
+        row_a = a.A[s:s + dim]
+        assert np.all(row_a == row_a[0]) and row_a[0] > 0
+        # permuting the columns permutes the weights and leaves the accumulator alone
+        assert np.array_equal(b.A[s:s + dim], row_a)
+        assert np.array_equal(b.W[s:s + dim], a.W[s:s + dim][perm])
+
+
 def _torch_reference_step(tables, B, offsets, keys, grad, W, opt_name):
     """Independent reference: torch embedding_bag (float64, sparse grads) + torch.optim."""
     outs, params = [], []

@@ -145,6 +145,8 @@ def _build_workloads() -> dict:
         name="skew",
         tables=tuple(TableSpec(5_000_000, d, "f32", "sum", "sgd", 0.01) for d in (16, 32, 64, 128) * 2),
         batch=262144, hot_kind="fixed", hot_lo=50, hot_hi=50, key_dist="zipf", alpha=1.5)
+    # the dlrm workload with one Adagrad accumulator per row instead of per element
+    w["dlrm_rowwise"] = w["dlrm"].replace(name="dlrm_rowwise").with_tables(opt="rowwise_adagrad")
     return w
 
 

@@ -22,7 +22,7 @@ EMB_ERR_STATE = -7
 
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 POOLINGS = {"sum": 0, "mean": 1}
-OPTS = {"sgd": 0, "adagrad": 1}
+OPTS = {"sgd": 0, "adagrad": 1, "rowwise_adagrad": 2}
 VARIANTS = {"reduction": 0, "unique_sort": 1, "unique_hash": 2}
 
 # every symbol the header declares

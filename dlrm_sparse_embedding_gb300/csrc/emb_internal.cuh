@@ -90,9 +90,13 @@ __device__ __forceinline__ void store_w4(void* w, int dtype, int64_t elem, float
     *reinterpret_cast<uint2*>(static_cast<unsigned short*>(w) + elem) = raw;
 }
 
-// One optimizer step on 4 consecutive elements of a row whose current values
-// (w, and a for Adagrad) have already been loaded.
-__device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t elem, const float g[4], float4 w, float4 a)
+// One optimizer step on 4 consecutive elements (starting at elem) of row
+// `row`, whose current values have been loaded: w, and the state a from
+// load_state4.  ssq is the sum over the whole row of G^2 (row-wise Adagrad
+// only; the caller reduces it over the lanes holding the row), and `writer`
+// says which one lane stores the row's accumulator.
+__device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t row, int64_t elem, const float g[4],
+                                              float4 w, float4 a, float ssq, bool writer)
 {
     float wv[4] = {w.x, w.y, w.z, w.w};
     if (tb.opt == EMB_OPT_ADAGRAD) {
@@ -104,6 +108,12 @@ __device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t elem, 
             wv[q] = __fmaf_rn(-tb.lr, __fdiv_rn(g[q], den), wv[q]);
         }
         *reinterpret_cast<float4*>(tb.state + elem) = make_float4(av[0], av[1], av[2], av[3]);
+    } else if (tb.opt == EMB_OPT_ROWWISE_ADAGRAD) {
+        const float an = __fadd_rn(a.x, __fdiv_rn(ssq, (float)tb.dim));
+        const float den = __fadd_rn(__fsqrt_rn(an), tb.eps);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) wv[q] = __fmaf_rn(-tb.lr, __fdiv_rn(g[q], den), wv[q]);
+        if (writer) tb.state[row] = an;
     } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) wv[q] = __fmaf_rn(-tb.lr, g[q], wv[q]);
@@ -111,11 +121,27 @@ __device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t elem, 
     store_w4(tb.w, tb.dtype, elem, make_float4(wv[0], wv[1], wv[2], wv[3]));
 }
 
-
-__device__ __forceinline__ float4 load_state4(const TableDev& tb, int64_t elem)
+// Optimizer state of the 4 elements at elem of row `row`: Adagrad's four
+// accumulators, row-wise Adagrad's one (in .x), nothing for SGD.
+__device__ __forceinline__ float4 load_state4(const TableDev& tb, int64_t row, int64_t elem)
 {
-    if (tb.opt != EMB_OPT_ADAGRAD) return make_float4(0.f, 0.f, 0.f, 0.f);
-    return *reinterpret_cast<const float4*>(tb.state + elem);
+    if (tb.opt == EMB_OPT_ADAGRAD) return *reinterpret_cast<const float4*>(tb.state + elem);
+    if (tb.opt == EMB_OPT_ROWWISE_ADAGRAD) return make_float4(tb.state[row], 0.f, 0.f, 0.f);
+    return make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Sum of squares of a lane's 4 gradient values.
+__device__ __forceinline__ float sq4(const float g[4])
+{
+    return __fmaf_rn(g[3], g[3], __fmaf_rn(g[2], g[2], __fmaf_rn(g[1], g[1], __fmul_rn(g[0], g[0]))));
+}
+
+// Sum of v over aligned groups of `width` lanes (a power of two) by an xor
+// butterfly: every lane of a group ends with the same bits.
+__device__ __forceinline__ float group_sum(float v, int width, uint32_t mask)
+{
+    for (int off = 1; off < width; off <<= 1) v = __fadd_rn(v, __shfl_xor_sync(mask, v, off));
+    return v;
 }
 
 // ---------------------------------------------------------------------------

@@ -142,6 +142,12 @@ void free_all(emb_layer* L)
 
 size_t dtype_bytes(int32_t dt) { return dt == EMB_F32 ? 4 : 2; }
 
+// fp32 optimizer state values per row: dim (Adagrad), 1 (row-wise Adagrad), 0 (SGD)
+int64_t state_cols(const TableDev& d)
+{
+    return d.opt == EMB_OPT_ADAGRAD ? d.dim : (d.opt == EMB_OPT_ROWWISE_ADAGRAD ? 1 : 0);
+}
+
 cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
 
 int track(emb_layer* L, int launched)
@@ -156,7 +162,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ------------------------------- kernels ----------------------------------
 
 __global__ void init_uniform_kernel(void* w, int dtype, int64_t rows, int dim, int t, uint64_t seed, float lo,
-                                    float hi, float* state, float init_acc)
+                                    float hi, float* state, int state_cols, float init_acc)
 {
     const int64_t total = rows * dim;
     const float d = __fsub_rn(hi, lo);
@@ -174,12 +180,12 @@ __global__ void init_uniform_kernel(void* w, int dtype, int64_t rows, int dim, i
         if (dtype == EMB_F32) static_cast<float*>(w)[e] = v;
         else if (dtype == EMB_F16) static_cast<__half*>(w)[e] = __float2half_rn(v);
         else static_cast<__nv_bfloat16*>(w)[e] = __float2bfloat16_rn(v);
-        if (state) state[e] = init_acc;
+        if (state && c < state_cols) state[r * state_cols + c] = init_acc;
     }
 }
 
-__global__ void gather_rows_kernel(const void* w, const float* state, int dtype, int64_t rows, int dim,
-                                   const int64_t* ids, int64_t n, void* wout, float* sout, int* err)
+__global__ void gather_rows_kernel(const void* w, const float* state, int state_cols, int dtype, int64_t rows,
+                                   int dim, const int64_t* ids, int64_t n, void* wout, float* sout, int* err)
 {
     const int64_t total = n * dim;
     const size_t eb = dtype == EMB_F32 ? 4 : 2;
@@ -194,7 +200,7 @@ __global__ void gather_rows_kernel(const void* w, const float* state, int dtype,
         const int64_t src = r * dim + c;
         if (eb == 4) static_cast<float*>(wout)[e] = static_cast<const float*>(w)[src];
         else static_cast<unsigned short*>(wout)[e] = static_cast<const unsigned short*>(w)[src];
-        if (sout && state) sout[e] = state[src];
+        if (sout && state && c < state_cols) sout[i * state_cols + c] = state[r * state_cols + c];
     }
 }
 
@@ -311,7 +317,7 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
     for (int t = 0; t < num_tables; ++t) {
         const emb_table_spec& s = specs[t];
         if (s.rows < 1 || s.dim < 4 || s.dim > kMaxDim || (s.dim & 3) || s.dtype < 0 || s.dtype > 2 ||
-            s.pooling < 0 || s.pooling > 1 || s.opt < 0 || s.opt > 1)
+            s.pooling < 0 || s.pooling > 1 || s.opt < 0 || s.opt > 2)
             return EMB_ERR_INVALID_ARG;
         total_rows += (uint64_t)s.rows;
         total_dim += s.dim;
@@ -350,7 +356,7 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
         d.w = nullptr;
         d.state = nullptr;
         ok = dalloc(L, &d.w, (size_t)s.rows * s.dim * dtype_bytes(s.dtype));
-        if (ok && s.opt == EMB_OPT_ADAGRAD) ok = dalloc_n(L, &d.state, s.rows * (int64_t)s.dim);
+        if (ok && state_cols(d) > 0) ok = dalloc_n(L, &d.state, s.rows * state_cols(d));
         rb += (uint64_t)s.rows;
         doff += s.dim;
     }
@@ -426,7 +432,7 @@ int emb_init_uniform(emb_layer* L, uint64_t seed, float lo, float hi, void* stre
         const TableDev& d = L->tabs[t];
         const int64_t total = d.rows * d.dim;
         init_uniform_kernel<<<grid_for(total, 256, 65536), 256, 0, S(stream)>>>(
-            d.w, d.dtype, d.rows, d.dim, t, seed, lo, hi, d.state, L->specs[t].init_acc);
+            d.w, d.dtype, d.rows, d.dim, t, seed, lo, hi, d.state, (int)state_cols(d), L->specs[t].init_acc);
         L->launches += 1;
     }
     return cudaGetLastError() == cudaSuccess ? EMB_OK : EMB_ERR_CUDA;
@@ -714,7 +720,7 @@ int emb_get_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, void* weights
     bool ok = cudaMemcpyAsync(weights_host, static_cast<char*>(d.w) + (size_t)row0 * d.dim * eb,
                               (size_t)n * d.dim * eb, cudaMemcpyDeviceToHost, st) == cudaSuccess;
     if (ok && state_host)
-        ok = cudaMemcpyAsync(state_host, d.state + (size_t)row0 * d.dim, sizeof(float) * (size_t)n * d.dim,
+        ok = cudaMemcpyAsync(state_host, d.state + (size_t)row0 * state_cols(d), sizeof(float) * (size_t)n * state_cols(d),
                              cudaMemcpyDeviceToHost, st) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
     return ok ? EMB_OK : EMB_ERR_CUDA;
@@ -732,7 +738,7 @@ int emb_set_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, const void* w
     bool ok = cudaMemcpyAsync(static_cast<char*>(d.w) + (size_t)row0 * d.dim * eb, weights_host,
                               (size_t)n * d.dim * eb, cudaMemcpyHostToDevice, st) == cudaSuccess;
     if (ok && state_host)
-        ok = cudaMemcpyAsync(d.state + (size_t)row0 * d.dim, state_host, sizeof(float) * (size_t)n * d.dim,
+        ok = cudaMemcpyAsync(d.state + (size_t)row0 * state_cols(d), state_host, sizeof(float) * (size_t)n * state_cols(d),
                              cudaMemcpyHostToDevice, st) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
     return ok ? EMB_OK : EMB_ERR_CUDA;
@@ -745,8 +751,8 @@ int emb_gather_rows(emb_layer* L, int32_t t, const int64_t* rows, int64_t n, voi
     const TableDev& d = L->tabs[t];
     if (state_out && !d.state) return EMB_ERR_INVALID_ARG;
     if (n == 0) return EMB_OK;
-    gather_rows_kernel<<<grid_for(n * d.dim, 256), 256, 0, S(stream)>>>(d.w, d.state, d.dtype, d.rows, d.dim, rows, n,
-                                                                        weights_out, state_out, L->err);
+    gather_rows_kernel<<<grid_for(n * d.dim, 256), 256, 0, S(stream)>>>(
+        d.w, d.state, (int)state_cols(d), d.dtype, d.rows, d.dim, rows, n, weights_out, state_out, L->err);
     L->launches += 1;
     return cudaGetLastError() == cudaSuccess ? EMB_OK : EMB_ERR_CUDA;
 }

@@ -169,12 +169,13 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
         const bool mean = tb.pooling == EMB_POOL_MEAN;
         const bool colok = 4 * li < tb.dim;
         float4 wv = make_float4(0.f, 0.f, 0.f, 0.f), av = wv;
-        int64_t elem = 0;
+        int64_t row = 0, elem = 0;
         if (!before && !after && colok && g == 0) {
             const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
-            elem = (int64_t)(gid - tb.row_base) * tb.dim + 4 * li;
+            row = (int64_t)(gid - tb.row_base);
+            elem = row * tb.dim + 4 * li;
             wv = load_w4(tb.w, tb.dtype, elem);
-            av = load_state4(tb, elem);
+            av = load_state4(tb, row, elem);
         }
         float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
         if (colok) {
@@ -201,16 +202,18 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
                 kahan_add(s[k], c[k], -oc);
             }
         }
-        if (g == 0 && colok) {
-            float gs[4];
+        float gs[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) gs[k] = __fsub_rn(s[k], c[k]);
-            if (before || after) {
+        for (int k = 0; k < 4; ++k) gs[k] = __fsub_rn(s[k], c[k]);
+        if (before || after) {
+            if (g == 0 && colok) {
                 float* sp = slot_ptr(a.slots, chunk, before ? kSlotHead : kSlotTail);
                 *reinterpret_cast<float4*>(sp + 4 * li) = make_float4(gs[0], gs[1], gs[2], gs[3]);
-            } else {
-                apply_update4(tb, elem, gs, wv, av);
             }
+        } else {
+            // row-wise Adagrad needs the whole row's sum of squares (every group holds the row)
+            const float ssq = tb.opt == EMB_OPT_ROWWISE_ADAGRAD ? group_sum(sq4(gs), Lg, 0xffffffffu) : 0.f;
+            if (g == 0 && colok) apply_update4(tb, row, elem, gs, wv, av, ssq, li == 0);
         }
         if (after && !before && lane == 0) a.split_list[atomicAdd(a.split_count, 1)] = (uint32_t)chunk;
         return;
@@ -230,12 +233,13 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
         const bool colok = 4 * li < tb.dim;
         // a run applied here loads its row now, overlapping the gradient gathers
         float4 wv = make_float4(0.f, 0.f, 0.f, 0.f), av = wv;
-        int64_t elem = 0;
+        int64_t row = 0, elem = 0;
         if (!before && !after && colok) {
             const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
-            elem = (int64_t)(gid - tb.row_base) * tb.dim + 4 * li;
+            row = (int64_t)(gid - tb.row_base);
+            elem = row * tb.dim + 4 * li;
             wv = load_w4(tb.w, tb.dtype, elem);
-            av = load_state4(tb, elem);
+            av = load_state4(tb, row, elem);
         }
         float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
         if (colok) {
@@ -259,15 +263,19 @@ __global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a
                 kahan_add(s[2], c[2], ta.z);
                 kahan_add(s[3], c[3], ta.w);
             }
-            float gs[4];
+        }
+        float gs[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) gs[k] = __fsub_rn(s[k], c[k]);
-            if (before || after) {
+        for (int k = 0; k < 4; ++k) gs[k] = __fsub_rn(s[k], c[k]);
+        if (before || after) {
+            if (colok) {
                 float* sp = slot_ptr(a.slots, chunk, before ? kSlotHead : kSlotTail);
                 *reinterpret_cast<float4*>(sp + 4 * li) = make_float4(gs[0], gs[1], gs[2], gs[3]);
-            } else {
-                apply_update4(tb, elem, gs, wv, av);
             }
+        } else {
+            // row-wise Adagrad needs the whole row's sum of squares, held by the group's lanes
+            const float ssq = tb.opt == EMB_OPT_ROWWISE_ADAGRAD ? group_sum(sq4(gs), Lg, gmask) : 0.f;
+            if (colok) apply_update4(tb, row, elem, gs, wv, av, ssq, li == 0);
         }
         // the chunk where a split run starts registers it for the combine kernel
         if (after && !before && li == 0) a.split_list[atomicAdd(a.split_count, 1)] = (uint32_t)chunk;
@@ -340,18 +348,24 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
         for (int q = 0; q < 4; ++q) part[warp][4 * lane + q] = __fsub_rn(s[q], cc4[q]);
     }
     __syncthreads();
-    if (warp == 0 && colok) {
+    if (warp == 0) {
         float gs[4] = {0.f, 0.f, 0.f, 0.f}, gc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int w = 0; w < W; ++w) {
+        if (colok) {
+            for (int w = 0; w < W; ++w) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) kahan_add(gs[q], gc[q], part[w][4 * lane + q]);
+                for (int q = 0; q < 4; ++q) kahan_add(gs[q], gc[q], part[w][4 * lane + q]);
+            }
         }
         float g[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) g[q] = __fsub_rn(gs[q], gc[q]);
-        const uint32_t gid = a.gid_of_key ? a.gid_of_key[key] : key;
-        const int64_t elem = (int64_t)(gid - tb.row_base) * tb.dim + 4 * lane;
-        apply_update4(tb, elem, g, load_w4(tb.w, tb.dtype, elem), load_state4(tb, elem));
+        const float ssq = tb.opt == EMB_OPT_ROWWISE_ADAGRAD ? group_sum(sq4(g), 32, 0xffffffffu) : 0.f;
+        if (colok) {
+            const uint32_t gid = a.gid_of_key ? a.gid_of_key[key] : key;
+            const int64_t row = (int64_t)(gid - tb.row_base);
+            const int64_t elem = row * tb.dim + 4 * lane;
+            apply_update4(tb, row, elem, g, load_w4(tb.w, tb.dtype, elem), load_state4(tb, row, elem), ssq, lane == 0);
+        }
     }
 }
 

@@ -37,12 +37,18 @@ def _spec_field(s, name, default=None):
     return v if v is not None else default
 
 
+def state_cols(spec) -> int:
+    """fp32 optimizer state values per row: dim (Adagrad), 1 (row-wise Adagrad), 0 (SGD)."""
+    opt = _spec_field(spec, "opt", "sgd")
+    return int(spec.dim) if opt == "adagrad" else (1 if opt == "rowwise_adagrad" else 0)
+
+
 class EmbeddingLayer:
     """Multi-table embedding layer resident on the current CUDA device.
 
     ``tables``: sequence of objects with ``rows, dim`` and optionally
     ``dtype`` ("f32"/"f16"/"bf16"), ``pooling`` ("sum"/"mean"), ``opt``
-    ("sgd"/"adagrad"), ``lr``, ``eps``, ``init_acc``.
+    ("sgd"/"adagrad"/"rowwise_adagrad"), ``lr``, ``eps``, ``init_acc``.
     """
 
     def __init__(self, tables: Sequence, max_batch: int, max_nnz: int):
@@ -129,12 +135,14 @@ class EmbeddingLayer:
         return (uniq[:u], None if inv is None else inv[:m], cnt[:u], seg[:u + 1], bags[:m])
 
     # -- rows -----------------------------------------------------------------
+    # State arrays have state_cols(spec) columns: dim (Adagrad), 1 (row-wise
+    # Adagrad); SGD tables have none.
     def gather_rows(self, t: int, rows: torch.Tensor, with_state: bool = False, stream=None):
         spec = self.tables[t]
         dt = _spec_field(spec, "dtype", "f32")
         n = int(rows.numel())
         w = torch.empty((n, int(spec.dim)), dtype=_TORCH_WDTYPE[dt], device=rows.device)
-        s = torch.empty((n, int(spec.dim)), dtype=torch.float32, device=rows.device) if with_state else None
+        s = torch.empty((n, state_cols(spec)), dtype=torch.float32, device=rows.device) if with_state else None
         check(lib.emb_gather_rows(self._h, t, _ptr(rows), n, _ptr(w), _ptr(s), _stream(stream)), "emb_gather_rows")
         return w, s
 
@@ -142,7 +150,7 @@ class EmbeddingLayer:
         spec = self.tables[t]
         dt = _spec_field(spec, "dtype", "f32")
         w = np.empty((n, int(spec.dim)), dtype=_NP_WDTYPE[dt])
-        s = np.empty((n, int(spec.dim)), dtype=np.float32) if with_state else None
+        s = np.empty((n, state_cols(spec)), dtype=np.float32) if with_state else None
         check(lib.emb_get_rows(self._h, t, row0, n, w.ctypes.data_as(ctypes.c_void_p),
                                None if s is None else s.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
               "emb_get_rows")
@@ -153,6 +161,8 @@ class EmbeddingLayer:
         dt = _spec_field(spec, "dtype", "f32")
         w = np.ascontiguousarray(weights, dtype=_NP_WDTYPE[dt])
         s = None if state is None else np.ascontiguousarray(state, dtype=np.float32)
+        if s is not None and s.size != w.shape[0] * state_cols(spec):
+            raise ValueError("state must hold %d values per row" % state_cols(spec))
         check(lib.emb_set_rows(self._h, t, row0, w.shape[0], w.ctypes.data_as(ctypes.c_void_p),
                                None if s is None else s.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
               "emb_set_rows")

@@ -53,7 +53,11 @@ typedef enum {
 
 typedef enum { EMB_F32 = 0, EMB_F16 = 1, EMB_BF16 = 2 } emb_dtype;
 typedef enum { EMB_POOL_SUM = 0, EMB_POOL_MEAN = 1 } emb_pooling;
-typedef enum { EMB_OPT_SGD = 0, EMB_OPT_ADAGRAD = 1 } emb_opt;
+typedef enum {
+    EMB_OPT_SGD = 0,
+    EMB_OPT_ADAGRAD = 1,            /* one fp32 accumulator per element */
+    EMB_OPT_ROWWISE_ADAGRAD = 2     /* one fp32 accumulator per row */
+} emb_opt;
 typedef enum {
     EMB_BWD_REDUCTION = 0,      /* RB: sort (row id, bag) pairs, reduce each run of equal ids */
     EMB_BWD_UNIQUE_SORT = 1,    /* UB: sort-based dedup to unique/inverse/counts first, then reduce */
@@ -61,9 +65,10 @@ typedef enum {
 } emb_bwd_variant;
 
 /* One embedding table.  dim must be a multiple of 4 in [4, 128]; rows >= 1.
- * lr / eps / init_acc: SGD uses lr; Adagrad uses all three (init_acc is the
- * initial accumulator value).  The layer stores weights in `dtype` and the
- * Adagrad accumulator in fp32; all arithmetic is fp32. */
+ * lr / eps / init_acc: SGD uses lr; both Adagrads use all three (init_acc is
+ * the initial accumulator value).  The layer stores weights in `dtype` and the
+ * accumulators in fp32 (rows*dim of them for Adagrad, rows for row-wise
+ * Adagrad); all arithmetic is fp32. */
 typedef struct {
     int64_t rows;
     int32_t dim;
@@ -124,6 +129,11 @@ int emb_forward(emb_layer* layer, const int64_t* keys, const int64_t* offsets,
  * then one optimizer step per touched row u (untouched rows are not read):
  *   SGD:     W <- W - lr*G
  *   Adagrad: A <- A + G*G ; W <- W - lr*G/(sqrt(A)+eps)     (per element)
+ *   row-wise Adagrad: a <- a + (1/dim) * sum_c G[c]^2 (one accumulator a per
+ *            row) ; W <- W - lr*G/(sqrt(a)+eps).  The pages name only the
+ *            fp32 optimizer; this is the row-wise form of the open DLRM
+ *            embedding libraries, which moves 4 bytes of state per row
+ *            instead of 4*dim.
  * fp32 math, W stored back rounded to nearest-even into its dtype.
  * grad_out: fp32[batch, sum(dim)], caller-owned, same layout as `out`.
  * variant: emb_bwd_variant.  All variants give the same indices and the same
@@ -204,7 +214,8 @@ int emb_unique_noalloc(const int64_t* keys, int64_t n, int64_t* unique, int32_t*
 /* Copy rows [row0, row0+n) of table t between the layer and host memory.
  * weights_host holds n*dim values of the table dtype (fp32, or the raw 16-bit
  * patterns of fp16/bf16); state_host (nullable; Adagrad tables only) n*dim
- * fp32.  Synchronous: the call waits for `stream`. */
+ * fp32, or n fp32 for row-wise Adagrad.  Synchronous: the call waits for
+ * `stream`. */
 int emb_get_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n, void* weights_host,
                  float* state_host, void* stream);
 int emb_set_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n,
@@ -212,7 +223,7 @@ int emb_set_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n,
 
 /* Gather n arbitrary rows (device int64 ids, each in [0, rows_t)) of table t
  * into device buffers: weights_out n*dim of the table dtype, state_out
- * (nullable) n*dim fp32.  Asynchronous.  Out-of-range ids are skipped and
+ * (nullable) n*dim fp32 (row-wise Adagrad: n fp32).  Asynchronous.  Out-of-range ids are skipped and
  * flagged like bad keys. */
 int emb_gather_rows(emb_layer* layer, int32_t t, const int64_t* rows, int64_t n,
                     void* weights_out, float* state_out, void* stream);

@@ -94,7 +94,7 @@ def gather_rows(layer, w: ci.Workload, t: int, rows: np.ndarray):
     import torch
     spec = w.tables[t]
     r = torch.from_numpy(np.ascontiguousarray(rows, dtype=np.int64)).cuda()
-    W, A = layer.gather_rows(t, r, with_state=spec.opt == "adagrad")
+    W, A = layer.gather_rows(t, r, with_state=spec.opt != "sgd")
     return to_f64(W, spec.dtype), None if A is None else A.double().cpu().numpy()
 
 
@@ -108,3 +108,13 @@ def expected_sorted_bags(gids: np.ndarray, bag_of_pos: np.ndarray) -> np.ndarray
 def bag_of_positions(offsets: np.ndarray) -> np.ndarray:
     lens = np.diff(offsets)
     return np.repeat(np.arange(lens.size, dtype=np.int64), lens)
+
+
+def ref_state(spec, A: np.ndarray, A_scale: np.ndarray, idx: np.ndarray):
+    """The oracle's accumulators (and scales) for the rows whose element
+    indices are `idx` [n, dim], shaped like the layer's state: [n, dim] for
+    Adagrad, [n, 1] for row-wise Adagrad (the oracle repeats the row's value
+    in every column)."""
+    if spec.opt == "rowwise_adagrad":
+        return A[idx[:, :1]], A_scale[idx[:, :1]]
+    return A[idx], A_scale[idx]

@@ -17,7 +17,7 @@ import pytest
 
 import ctr_inputs as ci
 import oracle
-from helpers import TOL, gather_rows, max_rel_err
+from helpers import TOL, gather_rows, max_rel_err, ref_state
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -45,7 +45,7 @@ def _built():
     _CACHE.clear()
 
 
-CASES = [("dlrm", "reduction"), ("dlrm", "unique_hash"), ("multihot", "reduction"), ("huge", "reduction"),
+CASES = [("dlrm", "reduction"), ("dlrm", "unique_hash"), ("dlrm_rowwise", "reduction"), ("multihot", "reduction"), ("huge", "reduction"),
          ("skew", "reduction"), ("skew", "unique_sort"), ("skew", "unique_hash")]
 
 
@@ -124,8 +124,9 @@ def test_fullsize_sampled_parity(name, variant):
             gw, ga = gather_rows(layer, w, t, st.row[sel])
             idx = st.row_start[sel][:, None] + np.arange(spec.dim)[None, :]
             assert max_rel_err(gw, W[idx], Ws[idx]) <= TOL[spec.dtype], (name, variant, t)
-            if spec.opt == "adagrad":
-                assert max_rel_err(ga, A[idx], As[idx]) <= 1e-5, (name, variant, t)
+            if spec.opt != "sgd":
+                ra, rs = ref_state(spec, A, As, idx)
+                assert max_rel_err(ga, ra, rs) <= 1e-5, (name, variant, t)
 
         # ---- untouched rows keep their initial values ----
         rb = oracle.row_base([s.rows for s in w.tables])

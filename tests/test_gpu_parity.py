@@ -14,7 +14,7 @@ import pytest
 import ctr_inputs as ci
 import oracle
 from helpers import (TOL, bag_of_positions, expected_sorted_bags, gather_rows, init_rows_fn, max_rel_err,
-                     run_gpu_step)
+                     ref_state, run_gpu_step)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,8 +34,9 @@ def _small(name):
     base = ci.workload(name if name in ci.WORKLOADS else name.split("_")[0])
     if name == "tiny":
         return base
-    if name == "dlrm_small":
-        tabs = tuple(ci.TableSpec(min(t.rows, 200_000), t.dim, t.dtype, t.pooling, t.opt, t.lr, t.eps)
+    if name in ("dlrm_small", "dlrm_small_rowwise"):
+        opt = "rowwise_adagrad" if name.endswith("rowwise") else None
+        tabs = tuple(ci.TableSpec(min(t.rows, 200_000), t.dim, t.dtype, t.pooling, opt or t.opt, t.lr, t.eps)
                      for t in base.tables)
         return base.replace(name=name, tables=tabs, batch=4096)
     if name == "multihot_small":
@@ -73,8 +74,9 @@ def check_step(w, batch, grad, variant, seed=0, expect_status=0, sample_untouche
             W, A = gather_rows(layer, w, t, ref.rows.row[sel])
             idx = (ref.rows.row_start[sel][:, None] + np.arange(spec.dim)[None, :])
             assert max_rel_err(W, ref.W[idx], ref.W_scale[idx]) <= TOL[spec.dtype], (t, spec)
-            if spec.opt == "adagrad":
-                assert max_rel_err(A, ref.A[idx], ref.A_scale[idx]) <= 1e-5, t
+            if spec.opt != "sgd":
+                ra, rs = ref_state(spec, ref.A, ref.A_scale, idx)
+                assert max_rel_err(A, ra, rs) <= 1e-5, t
         # untouched rows keep their initial values exactly
         rng = np.random.default_rng(1)
         for t, spec in enumerate(w.tables):
@@ -95,8 +97,8 @@ def check_step(w, batch, grad, variant, seed=0, expect_status=0, sample_untouche
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("name", ["tiny", "dlrm_small", "multihot_small", "multihot_bf16", "huge_small",
-                                  "skew_small"])
+@pytest.mark.parametrize("name", ["tiny", "dlrm_small", "dlrm_small_rowwise", "multihot_small", "multihot_bf16",
+                                  "huge_small", "skew_small"])
 def test_step_parity(name, variant):
     w = _small(name)
     batch = ci.make_batch(w)
@@ -108,16 +110,17 @@ def test_init_matches_counter_generator_bit_exactly():
     import torch
     from dlrm_sparse_embedding_gb300 import EmbeddingLayer
     tabs = [ci.TableSpec(3000, 16, "f32"), ci.TableSpec(777, 64, "f16", opt="adagrad", init_acc=0.1),
-            ci.TableSpec(5000, 128, "bf16")]
+            ci.TableSpec(5000, 128, "bf16"), ci.TableSpec(901, 12, "f32", opt="rowwise_adagrad", init_acc=0.1)]
     layer = EmbeddingLayer(tabs, 8, 16)
     try:
         layer.init_uniform(12345, -0.05, 0.05)
         for t, s in enumerate(tabs):
-            W, A = layer.get_rows(t, 0, s.rows, with_state=s.opt == "adagrad")
+            W, A = layer.get_rows(t, 0, s.rows, with_state=s.opt != "sgd")
             ref = ci.init_values(12345, t, np.arange(s.rows), s.dim, -0.05, 0.05, s.dtype)
             assert np.array_equal(W.view(np.uint16) if s.dtype != "f32" else W,
                                   ref.view(np.uint16) if s.dtype == "f16" else ref)
             if A is not None:
+                assert A.shape == (s.rows, s.dim if s.opt == "adagrad" else 1)
                 assert np.all(A == np.float32(0.1))
     finally:
         layer.close()
@@ -343,3 +346,25 @@ def test_early_dedup_is_bitwise_identical(early, bwd):
     (o0, d0, r0), (o1, d1, r1) = res
     for a, b in zip(o0 + d0 + r0, o1 + d1 + r1):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_rowwise_adagrad_dims_pooling_and_split_rows(variant):
+    # row-wise Adagrad on narrow, odd and full-width rows (lanes past the row's
+    # end take part in the row's sum of squares with zeros), mean pooling,
+    # 16-bit storage, and one row hit by a third of the lookups, so it is split
+    # over many chunks and finished by the combine kernel
+    tabs = [ci.TableSpec(2000, 20, "f32", "mean", "rowwise_adagrad", 0.01, 1e-8, 0.05),
+            ci.TableSpec(500, 100, "bf16", "sum", "rowwise_adagrad", 0.02, 1e-8, 0.0),
+            ci.TableSpec(3000, 4, "f16", "sum", "rowwise_adagrad", 0.01, 1e-6, 0.0),
+            ci.TableSpec(50, 128, "f32", "sum", "rowwise_adagrad", 0.01, 1e-8, 0.1)]
+    B = 1500
+    lens = np.random.default_rng(6).integers(0, 12, size=len(tabs) * B)
+
+    def keys(rng, t, s, L):
+        k = rng.integers(0, s.rows, L)
+        k[rng.random(L) < 0.33] = s.rows // 2
+        return k
+
+    w, b, g = _custom(tabs, B, lens, keys, seed=8)
+    check_step(w, b, g, variant)

@@ -222,6 +222,7 @@ struct ReduceArgs {
     float* slots;               // [nchunks][2][kMaxDim]
     uint32_t* split_list;       // [nchunks] chunks where a split run starts
     int* split_count;
+    int32_t max_dim;            // widest table of the layer (selects the chunk kernel's occupancy)
     int* err;
 };
 

@@ -595,6 +595,7 @@ int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, vo
     r.slots = L->slots;
     r.split_list = L->split_list;
     r.split_count = L->split_count;
+    r.max_dim = L->maxdim;
     r.err = L->err;
     int rc = EMB_OK;
     L->dedup_valid = false;

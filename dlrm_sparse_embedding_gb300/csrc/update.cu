@@ -36,7 +36,7 @@ namespace emb {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;   // chunk kernel block (small blocks recycle as soon as their chunks finish)
 constexpr int kCombineThreads = 256;
 constexpr int kCombineBlocksPerSM = 4;
 
@@ -84,7 +84,12 @@ __device__ __forceinline__ float entry_factor(const ReduceArgs& a, const uint16_
     return mean ? __fmul_rn(f, __ldg(a.bag_scale + b)) : f;
 }
 
-__global__ void __launch_bounds__(kThreads, 4) reduce_update_chunks(ReduceArgs a)
+// kMinBlocks: resident blocks per SM the registers are sized for.  Layers
+// with rows wider than 64 run one lane group per warp and gain from more
+// warps in flight (10 blocks, 48 registers); narrower layers lose more to the
+// spills than they gain (8 blocks, 64 registers).
+template <int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(ReduceArgs a)
 {
     extern __shared__ uint32_t smem_runs[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -391,10 +396,17 @@ int launch_reduce_update(const ReduceArgs& a, cudaStream_t st)
     const int64_t threads = a.nchunks * 32;
     const unsigned blocks = (unsigned)((threads + kThreads - 1) / kThreads);
     const size_t smem = sizeof(uint32_t) * (size_t)(kThreads / 32) * (size_t)warp_words(a.chunk);
-    if (cudaFuncSetAttribute(reduce_update_chunks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return -1;
-    reduce_update_chunks<<<blocks, kThreads, smem, st>>>(a);
+    if (a.max_dim > 64) {
+        if (cudaFuncSetAttribute(reduce_update_chunks<10>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return -1;
+        reduce_update_chunks<10><<<blocks, kThreads, smem, st>>>(a);
+    } else {
+        if (cudaFuncSetAttribute(reduce_update_chunks<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return -1;
+        reduce_update_chunks<8><<<blocks, kThreads, smem, st>>>(a);
+    }
     int launched = 1;
     if (a.nchunks > 1) {
         int dev = 0, sms = 152;

@@ -53,6 +53,7 @@ class TableSpec:
     lr: float = 0.01
     eps: float = 1e-8
     init_acc: float = 0.0
+    master: bool = False        # keep an fp32 master copy (16-bit storage only)
 
 
 @dataclasses.dataclass(frozen=True)

@@ -81,8 +81,8 @@ def lib():
                                  _f32p, _f64p, _vp]
         L.ora_reduce_sampled.argtypes = [i32, i32, _i64p, _i64p, _i64p, i64, i32, _i32p, _i64p, _i32p,
                                          i64, _f32p, _f64p, _vp, _i64p]
-        L.ora_update.argtypes = [i64, _i32p, _i64p, _i32p, _i32p, _i32p, _f64p, _f64p,
-                                 _f64p, _vp, _f64p, _f64p, _vp, _vp]
+        L.ora_update.argtypes = [i64, _i32p, _i64p, _i32p, _i32p, _i32p, _i32p, _f64p, _f64p,
+                                 _f64p, _vp, _f64p, _f64p, _vp, _vp, _vp]
         _lib = L
     return _lib
 
@@ -201,10 +201,12 @@ class RowStore:
 
 def make_row_store(tables, gids_sorted: np.ndarray,
                    init_rows: Callable[[int, np.ndarray], np.ndarray],
-                   state_init: bool = False) -> RowStore:
+                   state_init: bool = False, fp32_values: bool = False) -> RowStore:
     """Row store of the rows `gids_sorted` (ascending global ids), filled with
     their stored values from init_rows(t, local_rows) decoded to binary64, or
-    with the tables' initial accumulator value when state_init is set."""
+    with the tables' initial accumulator value when state_init is set.  With
+    fp32_values, init_rows returns float32 values whatever the table's
+    storage type (an fp32 master copy)."""
     rows = np.array([t.rows for t in tables], dtype=np.int64)
     rb = row_base(rows)
     tab = (np.searchsorted(rb, gids_sorted, side="right") - 1).astype(np.int32)
@@ -222,7 +224,7 @@ def make_row_store(tables, gids_sorted: np.ndarray,
         if state_init:
             vals[idx] = float(np.float32(spec.init_acc))
         else:
-            vals[idx] = stored_to_f64(init_rows(t, loc[sel]), spec.dtype).reshape(-1)
+            vals[idx] = stored_to_f64(init_rows(t, loc[sel]), "f32" if fp32_values else spec.dtype).reshape(-1)
     return RowStore(tab, loc, start, vals)
 
 
@@ -270,20 +272,26 @@ def reduce_sampled(tables, B: int, offsets: np.ndarray, gids: np.ndarray, sample
 
 
 def update(tables, store_: RowStore, state: RowStore, G: np.ndarray, Gabs: Optional[np.ndarray]):
-    """a5: updated weights and accumulators (binary64 of the rounded values)
-    plus their magnitude scales.  Inputs are not modified."""
+    """a5: updated weights and accumulators (binary64 of the rounded values),
+    their magnitude scales, and the stored weights after the step.  For a
+    table with an fp32 master copy (``master`` set, 16-bit storage) `store_`
+    holds the master values, the returned weights are the new masters and
+    the stored weights are them rounded to the storage type; otherwise the
+    two are equal.  Inputs are not modified."""
     dims = np.array([t.dim for t in tables], dtype=np.int32)
     dt = np.array([_DTYPE_CODE[t.dtype] for t in tables], dtype=np.int32)
     opt = np.array([_OPT_CODE[t.opt] for t in tables], dtype=np.int32)
+    master = np.array([int(bool(getattr(t, "master", False))) for t in tables], dtype=np.int32)
     lr = np.array([float(np.float32(t.lr)) for t in tables], dtype=np.float64)
     eps = np.array([float(np.float32(t.eps)) for t in tables], dtype=np.float64)
     W = store_.vals.copy()
     A = state.vals.copy()
     Ws = np.empty_like(W)
     As = np.empty_like(A)
-    lib().ora_update(store_.row_start.shape[0], store_.table, store_.row_start, dims, dt, opt, lr, eps,
-                     np.ascontiguousarray(G, np.float64), _ptr(Gabs), W, A, _ptr(Ws), _ptr(As))
-    return W, A, Ws, As
+    W16 = np.empty_like(W)
+    lib().ora_update(store_.row_start.shape[0], store_.table, store_.row_start, dims, dt, opt, master, lr, eps,
+                     np.ascontiguousarray(G, np.float64), _ptr(Gabs), W, A, _ptr(Ws), _ptr(As), _ptr(W16))
+    return W, A, Ws, As, W16
 
 
 @dataclasses.dataclass
@@ -298,6 +306,7 @@ class StepResult:
     out_scale: np.ndarray
     rows: RowStore          # initial values of the touched rows
     W: np.ndarray           # updated weights (binary64 of stored values), row store layout
+    M: np.ndarray           # updated fp32 masters (tables with one; elsewhere equal to W)
     A: np.ndarray           # updated accumulators
     W_scale: np.ndarray
     A_scale: np.ndarray
@@ -306,13 +315,24 @@ class StepResult:
 
 
 def step(tables, B: int, offsets, keys, table_ids, grad_out,
-         init_rows: Callable[[int, np.ndarray], np.ndarray]) -> StepResult:
-    """One full training step a1..a5 over a batch, on the touched rows only."""
+         init_rows: Callable[[int, np.ndarray], np.ndarray],
+         init_master: Optional[Callable[[int, np.ndarray], np.ndarray]] = None) -> StepResult:
+    """One full training step a1..a5 over a batch, on the touched rows only.
+    Tables with an fp32 master copy take its initial values from
+    init_master(t, local_rows) (float32); the forward reads the stored rows."""
     gids, bad = global_ids(tables, B, offsets, keys, table_ids)
     uniq, inv, cnt, seg = unique(gids, skip_negative=True)
     rows = make_row_store(tables, uniq, init_rows)
+    has_master = [bool(getattr(t, "master", False)) and t.dtype != "f32" for t in tables]
+    upd_rows = rows
+    if any(has_master):
+        if init_master is None:
+            raise ValueError("tables with an fp32 master copy need init_master")
+        upd_rows = make_row_store(tables, uniq, lambda t, r: init_master(t, r) if has_master[t] else
+                                  stored_to_f64(init_rows(t, r), tables[t].dtype).astype(np.float32),
+                                  fp32_values=True)
     state = make_row_store(tables, uniq, init_rows, state_init=True)
     out, oscale = forward(tables, B, offsets, inv, rows, want_scale=True)
     G, Gabs = reduce(tables, B, offsets, inv, rows, grad_out)
-    W, A, Ws, As = update(tables, rows, state, G, Gabs)
-    return StepResult(gids, bad, uniq, inv, cnt, seg, out, oscale, rows, W, A, Ws, As, G, Gabs)
+    M, A, Ws, As, W = update(tables, upd_rows, state, G, Gabs)
+    return StepResult(gids, bad, uniq, inv, cnt, seg, out, oscale, rows, W, M, A, Ws, As, G, Gabs)

@@ -26,6 +26,11 @@
  *    accumulator per row and adds the mean over the row's columns of G*G to
  *    it: A <- A + (1/dim) * sum_c G_c^2 ; W <- W - lr*G/(sqrt(A)+eps) (the
  *    form used by the open DLRM embedding libraries; the pages do not define it).
+ *  - GTC 2022 HugeCTR slides, "WEIGHT CONVERSION FOR MIXED PRECISION
+ *    TRAINING": the optimizer works on FP32 weights and the FP16 copy the
+ *    forward reads is converted from them.  A table with an fp32 master copy
+ *    updates the master in fp32 and stores the 16-bit weight as the master
+ *    rounded to nearest-even.
  *  - Duplicate keys in one batch: their gradients are summed first and each
  *    touched row gets exactly one optimizer step per batch.
  *
@@ -316,12 +321,17 @@ void ora_reduce_sampled(int32_t T, int32_t B, const int64_t* offsets, const int6
  * back as the binary64 value of the rounded result.  Wscale/Ascale
  * (nullable) receive the magnitude scales |W| + lr*Gabs/(sqrt(A')+eps) (SGD:
  * |W| + lr*Gabs) and A + Gabs^2 (row-wise: a + (1/dim) sum_c Gabs_c^2) used
- * to judge rounding error. */
+ * to judge rounding error.
+ * master (nullable): for tables with master[t] set (16-bit storage), W holds
+ * the fp32 master values; W' is rounded to fp32 as the new master and the
+ * stored 16-bit weight is that master rounded to the storage type.  W16
+ * (nullable) receives the stored weight after the step for every row (the
+ * same as W for tables without a master). */
 void ora_update(int64_t U, const int32_t* row_table, const int64_t* row_start,
                 const int32_t* dims, const int32_t* dtype, const int32_t* opt,
-                const double* lr, const double* eps,
+                const int32_t* master, const double* lr, const double* eps,
                 const double* G, const double* Gabs, double* W, double* A,
-                double* Wscale, double* Ascale)
+                double* Wscale, double* Ascale, double* W16)
 {
     for (int64_t k = 0; k < U; ++k) {
         int32_t t = row_table[k];
@@ -358,9 +368,17 @@ void ora_update(int64_t U, const int32_t* row_table, const int64_t* row_start,
                 step_scale = Gabs ? lr[t] * Gabs[base + c] : 0.0;
             }
             if (Wscale) Wscale[base + c] = fabs(w) + step_scale;
-            if (dtype[t] == 1) wn = ora_f16_to_f64(ora_round_f16(wn));
-            else if (dtype[t] == 2) wn = ora_bf16_to_f64(ora_round_bf16(wn));
-            else wn = (double)(float)wn;
+            if (master && master[t] && dtype[t] != 0) {
+                wn = (double)(float)wn;   /* the new fp32 master */
+                if (W16)
+                    W16[base + c] = dtype[t] == 1 ? ora_f16_to_f64(ora_round_f16(wn))
+                                                  : ora_bf16_to_f64(ora_round_bf16(wn));
+            } else {
+                if (dtype[t] == 1) wn = ora_f16_to_f64(ora_round_f16(wn));
+                else if (dtype[t] == 2) wn = ora_bf16_to_f64(ora_round_bf16(wn));
+                else wn = (double)(float)wn;
+                if (W16) W16[base + c] = wn;
+            }
             W[base + c] = wn;
         }
     }

@@ -439,6 +439,59 @@ def test_rowwise_adagrad_accumulator_is_one_value_per_row_and_column_order_free(
         assert np.array_equal(b.W[s:s + dim], a.W[s:s + dim][perm])
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("opt", ["sgd", "adagrad", "rowwise_adagrad"])
+def test_master_copy_follows_the_fp32_table(dtype, opt):
+    # the gradient does not depend on the weights (grad_out is given), so a
+    # 16-bit table's fp32 master must take exactly the fp32 table's steps, and
+    # its stored copy is that master rounded to nearest-even (NumPy's fp16
+    # conversion, torch's bf16 conversion)
+    rows, dim, B = 60, 8, 40
+    rng = np.random.default_rng(51)
+    keys = rng.integers(0, rows, B).astype(np.int64)
+    keys[:9] = 17
+    offsets = np.arange(B + 1, dtype=np.int64)
+    W0 = rng.uniform(-0.05, 0.05, (rows, dim)).astype(np.float32)
+    grad = rng.standard_normal((B, dim)).astype(np.float32)
+    tid = np.zeros(B, np.int32)
+    ref = oracle.step([_spec(rows, dim, "sum", opt)], B, offsets, keys, tid, grad, _dense_rows([W0]))
+    spec = ci.TableSpec(rows, dim, dtype, "sum", opt, 0.01, 1e-8, 0.0, master=True)
+    if dtype == "f16":
+        stored = W0.astype(np.float16)
+    else:
+        stored = torch.from_numpy(W0).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    res = oracle.step([spec], B, offsets, keys, tid, grad, lambda t, r: stored[r], lambda t, r: W0[r])
+    assert np.array_equal(res.M, ref.W)
+    assert np.array_equal(res.A, ref.A)
+    m32 = res.M.astype(np.float32)
+    if dtype == "f16":
+        want = m32.astype(np.float16).astype(np.float64)
+    else:
+        want = torch.from_numpy(m32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(res.W, want)
+
+
+def test_master_copy_keeps_a_step_below_half_a_16bit_ulp():
+    # fp16 spacing just below 1 is 2^-11.  A step of 2^-12 from 1.0 lands on the
+    # tie 1 - 2^-12, which rounds to the even neighbour 1.0: without a master
+    # the stored weight does not move; with one the master holds 1 - 2^-12 and
+    # the stored copy is 1.0.  Row 2, hit twice, moves by 2^-11 to 1 - 2^-11.
+    B = 3
+    lr = 2.0 ** -12
+    keys = np.array([1, 2, 2], dtype=np.int64)
+    offsets = np.arange(B + 1, dtype=np.int64)
+    W0 = np.ones((4, 4), dtype=np.float32)
+    grad = np.ones((B, 4), dtype=np.float32)
+    tid = np.zeros(B, np.int32)
+    plain = oracle.step([ci.TableSpec(4, 4, "f16", "sum", "sgd", lr)], B, offsets, keys, tid, grad,
+                        lambda t, r: W0.astype(np.float16)[r])
+    mast = oracle.step([ci.TableSpec(4, 4, "f16", "sum", "sgd", lr, master=True)], B, offsets, keys, tid, grad,
+                       lambda t, r: W0.astype(np.float16)[r], lambda t, r: W0[r])
+    assert plain.W.tolist() == [1.0] * 4 + [0.99951171875] * 4
+    assert mast.W.tolist() == [1.0] * 4 + [0.99951171875] * 4
+    assert mast.M.tolist() == [0.999755859375] * 4 + [0.99951171875] * 4
+
+
 def _torch_reference_step(tables, B, offsets, keys, grad, W, opt_name):
     """Independent reference: torch embedding_bag (float64, sparse grads) + torch.optim."""
     outs, params = [], []

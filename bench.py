@@ -45,6 +45,8 @@ CONFIG_TEXT = {
                  "Zipf(1.2), mean pooling, Adagrad"),
     "huge": ("single huge table: 1 fp16 table x 2e8 rows x dim 64, fp32 Adagrad state, batch 131,072, "
              "hotness 20, Zipf(1.1), sum pooling"),
+    "huge_master": ("single huge table with an fp32 master copy: 1 fp16 table x 2e8 rows x dim 64 plus fp32 master "
+                    "and fp32 Adagrad state, batch 131,072, hotness 20, Zipf(1.1), sum pooling"),
     "dlrm_rowwise": ("DLRM-style one-hot with row-wise Adagrad: 26 fp32 tables, rows log-uniform in [1e3,1e7], "
                      "dim 128, batch 65,536, hotness 1, Zipf(1.05) keys, sum pooling, one fp32 accumulator per row"),
     "skew": ("skewed dedup stress: 8 fp32 tables dims {16,32,64,128}x2 x 5e6 rows, batch 262,144, hotness 50, "
@@ -71,12 +73,15 @@ def algorithmic_bytes(w: ci.Workload, batch: ci.Batch, U_per_table: np.ndarray) 
     T, B, nnz = w.num_tables, w.batch, batch.nnz
     D = w.total_dim
     rows_bytes = sum(int(U_per_table[t]) * s.dim * _wbytes(s.dtype) for t, s in enumerate(w.tables))
+    # an fp32 master copy: the update reads and writes the master and writes the stored row
+    master_bytes = sum(int(U_per_table[t]) * s.dim * (8 - _wbytes(s.dtype))
+                       for t, s in enumerate(w.tables) if getattr(s, "master", False))
     state_cols = {"sgd": 0, "adagrad": None, "rowwise_adagrad": 1}
     state_bytes = sum(int(U_per_table[t]) * 4 * (s.dim if state_cols[s.opt] is None else state_cols[s.opt])
                       for t, s in enumerate(w.tables))
     fwd = 8 * nnz + 8 * (T * B + 1) + 4 * T * B + rows_bytes + 4 * B * D + 8 * nnz   # + gid/bag ids written
     dedup = 8 * nnz + 8 * nnz                                    # read (id, bag) pairs, write them sorted
-    upd = 4 * B * D + 8 * nnz + 2 * rows_bytes + 2 * state_bytes   # grad once, sorted ids+bags, row/state r+w
+    upd = 4 * B * D + 8 * nnz + 2 * rows_bytes + 2 * state_bytes + master_bytes   # grad once, sorted ids+bags, row/state r+w
     return {"forward": fwd, "dedup": dedup, "reduce_update": upd, "step": fwd + dedup + upd}
 
 
@@ -445,7 +450,8 @@ def main():
                             else "inside the backward",
                    "l2": "inputs larger than L2 (tables %.1f GB; out, grad_out %.0f MB each)" % (
                        sum(s.rows * (s.dim * _wbytes(s.dtype) + 4 * {"sgd": 0, "adagrad": s.dim,
-                                                                       "rowwise_adagrad": 1}[s.opt])
+                                                                       "rowwise_adagrad": 1}[s.opt]
+                                     + (4 * s.dim if getattr(s, "master", False) else 0))
                            for s in w.tables) / 1e9, w.batch * w.total_dim * 4 / 1e6),
                    "parallelism": "replicas x%d" % ws},
         "hbm": {"algorithmic_bytes_per_step": bytes_["step"], "achieved_gbs": step_gbs, "peak_gbs": peak,

@@ -148,6 +148,8 @@ def _build_workloads() -> dict:
         batch=262144, hot_kind="fixed", hot_lo=50, hot_hi=50, key_dist="zipf", alpha=1.5)
     # the dlrm workload with one Adagrad accumulator per row instead of per element
     w["dlrm_rowwise"] = w["dlrm"].replace(name="dlrm_rowwise").with_tables(opt="rowwise_adagrad")
+    # the huge fp16 table with an fp32 master copy
+    w["huge_master"] = w["huge"].replace(name="huge_master").with_tables(master=True)
     return w
 
 

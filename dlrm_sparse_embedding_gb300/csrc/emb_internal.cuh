@@ -29,7 +29,8 @@ constexpr uint32_t kNoSlot = 0xFFFFFFFEu;
 // Per-table metadata, resident in device memory.
 struct TableDev {
     void* w;             // rows x dim, dtype
-    float* state;        // rows x dim fp32 (Adagrad) or null
+    float* state;        // rows x dim fp32 (Adagrad), rows fp32 (row-wise Adagrad) or null
+    float* master;       // rows x dim fp32 master copy of a 16-bit table, or null
     int64_t rows;
     uint32_t row_base;   // global row id of row 0
     int32_t dim;
@@ -91,8 +92,9 @@ __device__ __forceinline__ void store_w4(void* w, int dtype, int64_t elem, float
 }
 
 // One optimizer step on 4 consecutive elements (starting at elem) of row
-// `row`, whose current values have been loaded: w, and the state a from
-// load_state4.  ssq is the sum over the whole row of G^2 (row-wise Adagrad
+// `row`, whose current values have been loaded: w (from load_update_w4), and
+// the state a from load_state4.  A table with a master copy gets the new
+// fp32 values there and their nearest-even rounding in the stored row.  ssq is the sum over the whole row of G^2 (row-wise Adagrad
 // only; the caller reduces it over the lanes holding the row), and `writer`
 // says which one lane stores the row's accumulator.
 __device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t row, int64_t elem, const float g[4],
@@ -118,7 +120,16 @@ __device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t row, i
 #pragma unroll
         for (int q = 0; q < 4; ++q) wv[q] = __fmaf_rn(-tb.lr, g[q], wv[q]);
     }
+    if (tb.master) *reinterpret_cast<float4*>(tb.master + elem) = make_float4(wv[0], wv[1], wv[2], wv[3]);
     store_w4(tb.w, tb.dtype, elem, make_float4(wv[0], wv[1], wv[2], wv[3]));
+}
+
+// The weights an update starts from: the fp32 master when the table has one,
+// else the stored row.
+__device__ __forceinline__ float4 load_update_w4(const TableDev& tb, int64_t elem)
+{
+    if (tb.master) return *reinterpret_cast<const float4*>(tb.master + elem);
+    return load_w4(tb.w, tb.dtype, elem);
 }
 
 // Optimizer state of the 4 elements at elem of row `row`: Adagrad's four

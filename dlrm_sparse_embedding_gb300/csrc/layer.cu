@@ -162,7 +162,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ------------------------------- kernels ----------------------------------
 
 __global__ void init_uniform_kernel(void* w, int dtype, int64_t rows, int dim, int t, uint64_t seed, float lo,
-                                    float hi, float* state, int state_cols, float init_acc)
+                                    float hi, float* state, int state_cols, float init_acc, float* master)
 {
     const int64_t total = rows * dim;
     const float d = __fsub_rn(hi, lo);
@@ -177,6 +177,7 @@ __global__ void init_uniform_kernel(void* w, int dtype, int64_t rows, int dim, i
         z ^= z >> 31;
         const float f = __fmul_rn(__uint2float_rn((uint32_t)(z >> 40)), 5.9604644775390625e-08f);
         const float v = __fadd_rn(lo, __fmul_rn(d, f));
+        if (master) master[e] = v;
         if (dtype == EMB_F32) static_cast<float*>(w)[e] = v;
         else if (dtype == EMB_F16) static_cast<__half*>(w)[e] = __float2half_rn(v);
         else static_cast<__nv_bfloat16*>(w)[e] = __float2bfloat16_rn(v);
@@ -317,7 +318,8 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
     for (int t = 0; t < num_tables; ++t) {
         const emb_table_spec& s = specs[t];
         if (s.rows < 1 || s.dim < 4 || s.dim > kMaxDim || (s.dim & 3) || s.dtype < 0 || s.dtype > 2 ||
-            s.pooling < 0 || s.pooling > 1 || s.opt < 0 || s.opt > 2)
+            s.pooling < 0 || s.pooling > 1 || s.opt < 0 || s.opt > 2 || s.master_fp32 < 0 || s.master_fp32 > 1 ||
+            (s.master_fp32 && s.dtype == EMB_F32))
             return EMB_ERR_INVALID_ARG;
         total_rows += (uint64_t)s.rows;
         total_dim += s.dim;
@@ -355,8 +357,10 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
         d.pad_ = 0;
         d.w = nullptr;
         d.state = nullptr;
+        d.master = nullptr;
         ok = dalloc(L, &d.w, (size_t)s.rows * s.dim * dtype_bytes(s.dtype));
         if (ok && state_cols(d) > 0) ok = dalloc_n(L, &d.state, s.rows * state_cols(d));
+        if (ok && s.master_fp32) ok = dalloc_n(L, &d.master, s.rows * (int64_t)s.dim);
         rb += (uint64_t)s.rows;
         doff += s.dim;
     }
@@ -432,7 +436,8 @@ int emb_init_uniform(emb_layer* L, uint64_t seed, float lo, float hi, void* stre
         const TableDev& d = L->tabs[t];
         const int64_t total = d.rows * d.dim;
         init_uniform_kernel<<<grid_for(total, 256, 65536), 256, 0, S(stream)>>>(
-            d.w, d.dtype, d.rows, d.dim, t, seed, lo, hi, d.state, (int)state_cols(d), L->specs[t].init_acc);
+            d.w, d.dtype, d.rows, d.dim, t, seed, lo, hi, d.state, (int)state_cols(d), L->specs[t].init_acc,
+            d.master);
         L->launches += 1;
     }
     return cudaGetLastError() == cudaSuccess ? EMB_OK : EMB_ERR_CUDA;
@@ -743,6 +748,44 @@ int emb_set_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, const void* w
                              cudaMemcpyHostToDevice, st) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
     return ok ? EMB_OK : EMB_ERR_CUDA;
+}
+
+int emb_get_master_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, float* master_host, void* stream)
+{
+    if (!L || t < 0 || t >= L->T || row0 < 0 || n < 0 || row0 + n > L->tabs[t].rows || (n > 0 && !master_host) ||
+        !L->tabs[t].master)
+        return EMB_ERR_INVALID_ARG;
+    const TableDev& d = L->tabs[t];
+    cudaStream_t st = S(stream);
+    const bool ok = cudaMemcpyAsync(master_host, d.master + (size_t)row0 * d.dim, sizeof(float) * (size_t)n * d.dim,
+                                    cudaMemcpyDeviceToHost, st) == cudaSuccess &&
+                    cudaStreamSynchronize(st) == cudaSuccess;
+    return ok ? EMB_OK : EMB_ERR_CUDA;
+}
+
+int emb_set_master_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, const float* master_host, void* stream)
+{
+    if (!L || t < 0 || t >= L->T || row0 < 0 || n < 0 || row0 + n > L->tabs[t].rows || (n > 0 && !master_host) ||
+        !L->tabs[t].master)
+        return EMB_ERR_INVALID_ARG;
+    const TableDev& d = L->tabs[t];
+    cudaStream_t st = S(stream);
+    const bool ok = cudaMemcpyAsync(d.master + (size_t)row0 * d.dim, master_host, sizeof(float) * (size_t)n * d.dim,
+                                    cudaMemcpyHostToDevice, st) == cudaSuccess &&
+                    cudaStreamSynchronize(st) == cudaSuccess;
+    return ok ? EMB_OK : EMB_ERR_CUDA;
+}
+
+int emb_gather_master_rows(emb_layer* L, int32_t t, const int64_t* rows, int64_t n, float* master_out, void* stream)
+{
+    if (!L || t < 0 || t >= L->T || n < 0 || (n > 0 && (!rows || !master_out)) || !L->tabs[t].master)
+        return EMB_ERR_INVALID_ARG;
+    if (n == 0) return EMB_OK;
+    const TableDev& d = L->tabs[t];
+    gather_rows_kernel<<<grid_for(n * d.dim, 256), 256, 0, S(stream)>>>(d.master, nullptr, 0, EMB_F32, d.rows, d.dim,
+                                                                        rows, n, master_out, nullptr, L->err);
+    L->launches += 1;
+    return cudaGetLastError() == cudaSuccess ? EMB_OK : EMB_ERR_CUDA;
 }
 
 int emb_gather_rows(emb_layer* L, int32_t t, const int64_t* rows, int64_t n, void* weights_out, float* state_out,

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
             const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
             row = (int64_t)(gid - tb.row_base);
             elem = row * tb.dim + 4 * li;
-            wv = load_w4(tb.w, tb.dtype, elem);
+            wv = load_update_w4(tb, elem);
             av = load_state4(tb, row, elem);
         }
         float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
             const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
             row = (int64_t)(gid - tb.row_base);
             elem = row * tb.dim + 4 * li;
-            wv = load_w4(tb.w, tb.dtype, elem);
+            wv = load_update_w4(tb, elem);
             av = load_state4(tb, row, elem);
         }
         float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -369,7 +369,7 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
             const uint32_t gid = a.gid_of_key ? a.gid_of_key[key] : key;
             const int64_t row = (int64_t)(gid - tb.row_base);
             const int64_t elem = row * tb.dim + 4 * lane;
-            apply_update4(tb, row, elem, g, load_w4(tb.w, tb.dtype, elem), load_state4(tb, row, elem), ssq, lane == 0);
+            apply_update4(tb, row, elem, g, load_update_w4(tb, elem), load_state4(tb, row, elem), ssq, lane == 0);
         }
     }
 }

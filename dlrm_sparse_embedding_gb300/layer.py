@@ -48,7 +48,8 @@ class EmbeddingLayer:
 
     ``tables``: sequence of objects with ``rows, dim`` and optionally
     ``dtype`` ("f32"/"f16"/"bf16"), ``pooling`` ("sum"/"mean"), ``opt``
-    ("sgd"/"adagrad"/"rowwise_adagrad"), ``lr``, ``eps``, ``init_acc``.
+    ("sgd"/"adagrad"/"rowwise_adagrad"), ``lr``, ``eps``, ``init_acc``,
+    ``master`` (keep an fp32 master copy of a 16-bit table).
     """
 
     def __init__(self, tables: Sequence, max_batch: int, max_nnz: int):
@@ -64,6 +65,7 @@ class EmbeddingLayer:
             arr[i].lr = float(_spec_field(s, "lr", 0.01))
             arr[i].eps = float(_spec_field(s, "eps", 1e-8))
             arr[i].init_acc = float(_spec_field(s, "init_acc", 0.0))
+            arr[i].master_fp32 = 1 if _spec_field(s, "master", False) else 0
         h = ctypes.c_void_p()
         check(lib.emb_create(arr, T, int(max_batch), int(max_nnz), ctypes.byref(h)), "emb_create")
         self._h = h
@@ -166,6 +168,26 @@ class EmbeddingLayer:
         check(lib.emb_set_rows(self._h, t, row0, w.shape[0], w.ctypes.data_as(ctypes.c_void_p),
                                None if s is None else s.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
               "emb_set_rows")
+
+    # -- fp32 master copies of 16-bit tables ------------------------------------
+    def gather_master_rows(self, t: int, rows: torch.Tensor, stream=None) -> torch.Tensor:
+        spec = self.tables[t]
+        n = int(rows.numel())
+        m = torch.empty((n, int(spec.dim)), dtype=torch.float32, device=rows.device)
+        check(lib.emb_gather_master_rows(self._h, t, _ptr(rows), n, _ptr(m), _stream(stream)),
+              "emb_gather_master_rows")
+        return m
+
+    def get_master_rows(self, t: int, row0: int, n: int, stream=None) -> np.ndarray:
+        m = np.empty((n, int(self.tables[t].dim)), dtype=np.float32)
+        check(lib.emb_get_master_rows(self._h, t, row0, n, m.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
+              "emb_get_master_rows")
+        return m
+
+    def set_master_rows(self, t: int, row0: int, master: np.ndarray, stream=None) -> None:
+        m = np.ascontiguousarray(master, dtype=np.float32).reshape(-1, int(self.tables[t].dim))
+        check(lib.emb_set_master_rows(self._h, t, row0, m.shape[0], m.ctypes.data_as(ctypes.c_void_p),
+                                      _stream(stream)), "emb_set_master_rows")
 
     # -- status ---------------------------------------------------------------
     def sync_status(self, stream=None) -> int:

@@ -68,7 +68,14 @@ typedef enum {
  * lr / eps / init_acc: SGD uses lr; both Adagrads use all three (init_acc is
  * the initial accumulator value).  The layer stores weights in `dtype` and the
  * accumulators in fp32 (rows*dim of them for Adagrad, rows for row-wise
- * Adagrad); all arithmetic is fp32. */
+ * Adagrad); all arithmetic is fp32.
+ * master_fp32 (fp16/bf16 tables only; EMB_ERR_INVALID_ARG for fp32): GTC 2022
+ * HugeCTR slides, "WEIGHT CONVERSION FOR MIXED PRECISION TRAINING" -- the
+ * optimizer keeps FP32 weights and the FP16 copy the forward reads is
+ * converted from them.  The layer then holds rows*dim fp32 master values;
+ * every update steps the master in fp32 and stores the 16-bit weight as the
+ * new master rounded to nearest-even, so steps smaller than half a 16-bit
+ * ulp accumulate instead of being rounded away. */
 typedef struct {
     int64_t rows;
     int32_t dim;
@@ -78,6 +85,7 @@ typedef struct {
     float lr;
     float eps;
     float init_acc;
+    int32_t master_fp32; /* 1: keep an fp32 master copy of a 16-bit table (see below); 0: none */
 } emb_table_spec;
 
 typedef struct emb_layer emb_layer;   /* opaque; owns tables, optimizer state and workspace */
@@ -220,6 +228,21 @@ int emb_get_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n, void* wei
                  float* state_host, void* stream);
 int emb_set_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n,
                  const void* weights_host, const float* state_host, void* stream);
+
+/* The fp32 master copy of rows [row0, row0+n) of table t (a table created
+ * with master_fp32 = 1; EMB_ERR_INVALID_ARG otherwise), n*dim fp32 in host
+ * memory, for checkpoints and tests.  Synchronous: the call waits for
+ * `stream`.  Setting the master does not touch the 16-bit weights: set both
+ * (emb_set_rows) to restore a checkpoint. */
+int emb_get_master_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n, float* master_host,
+                        void* stream);
+int emb_set_master_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n,
+                        const float* master_host, void* stream);
+/* Gather n arbitrary rows' master values (device int64 ids) into a device
+ * buffer of n*dim fp32.  Asynchronous; out-of-range ids are skipped and
+ * flagged like bad keys. */
+int emb_gather_master_rows(emb_layer* layer, int32_t t, const int64_t* rows, int64_t n, float* master_out,
+                           void* stream);
 
 /* Gather n arbitrary rows (device int64 ids, each in [0, rows_t)) of table t
  * into device buffers: weights_out n*dim of the table dtype, state_out

@@ -45,7 +45,7 @@ def _built():
     _CACHE.clear()
 
 
-CASES = [("dlrm", "reduction"), ("dlrm", "unique_hash"), ("dlrm_rowwise", "reduction"), ("multihot", "reduction"), ("huge", "reduction"),
+CASES = [("dlrm", "reduction"), ("dlrm", "unique_hash"), ("dlrm_rowwise", "reduction"), ("huge_master", "reduction"), ("multihot", "reduction"), ("huge", "reduction"),
          ("skew", "reduction"), ("skew", "unique_sort"), ("skew", "unique_hash")]
 
 
@@ -111,12 +111,19 @@ def test_fullsize_sampled_parity(name, variant):
         sample = uniq[pick]
         G, Gabs, count = oracle.reduce_sampled(w.tables, B, batch.offsets, gids, sample, grad)
         assert np.array_equal(count, cnt[pick])
-        st = oracle.make_row_store(w.tables, sample, lambda t, r: ci.init_values(
-            seed, t, r, w.tables[t].dim, w.w_lo, w.w_hi, w.tables[t].dtype))
+        # the update starts from the fp32 master where a table has one
+        def start_values(t, r):
+            spec = w.tables[t]
+            if spec.master:
+                return ci.init_values(seed, t, r, spec.dim, w.w_lo, w.w_hi, "f32")
+            return ci.stored_to_f64(ci.init_values(seed, t, r, spec.dim, w.w_lo, w.w_hi, spec.dtype),
+                                    spec.dtype).astype(np.float32)
+
+        st = oracle.make_row_store(w.tables, sample, start_values, fp32_values=True)
         state = oracle.make_row_store(w.tables, sample, None, state_init=True)
         Gflat = np.concatenate([G[q, :w.tables[st.table[q]].dim] for q in range(sample.size)])
         Gaflat = np.concatenate([Gabs[q, :w.tables[st.table[q]].dim] for q in range(sample.size)])
-        W, A, Ws, As = oracle.update(w.tables, st, state, Gflat, Gaflat)
+        M, A, Ws, As, W = oracle.update(w.tables, st, state, Gflat, Gaflat)
         for t, spec in enumerate(w.tables):
             sel = np.nonzero(st.table == t)[0]
             if sel.size == 0:
@@ -124,6 +131,9 @@ def test_fullsize_sampled_parity(name, variant):
             gw, ga = gather_rows(layer, w, t, st.row[sel])
             idx = st.row_start[sel][:, None] + np.arange(spec.dim)[None, :]
             assert max_rel_err(gw, W[idx], Ws[idx]) <= TOL[spec.dtype], (name, variant, t)
+            if spec.master:
+                gm = layer.gather_master_rows(t, torch.from_numpy(np.ascontiguousarray(st.row[sel])).cuda())
+                assert max_rel_err(gm.cpu().numpy(), M[idx], Ws[idx]) <= 1e-5, (name, variant, t)
             if spec.opt != "sgd":
                 ra, rs = ref_state(spec, A, As, idx)
                 assert max_rel_err(ga, ra, rs) <= 1e-5, (name, variant, t)

@@ -110,7 +110,8 @@ def test_init_matches_counter_generator_bit_exactly():
     import torch
     from dlrm_sparse_embedding_gb300 import EmbeddingLayer
     tabs = [ci.TableSpec(3000, 16, "f32"), ci.TableSpec(777, 64, "f16", opt="adagrad", init_acc=0.1),
-            ci.TableSpec(5000, 128, "bf16"), ci.TableSpec(901, 12, "f32", opt="rowwise_adagrad", init_acc=0.1)]
+            ci.TableSpec(5000, 128, "bf16"), ci.TableSpec(901, 12, "f32", opt="rowwise_adagrad", init_acc=0.1),
+            ci.TableSpec(640, 32, "bf16", opt="adagrad", init_acc=0.1, master=True)]
     layer = EmbeddingLayer(tabs, 8, 16)
     try:
         layer.init_uniform(12345, -0.05, 0.05)
@@ -122,6 +123,9 @@ def test_init_matches_counter_generator_bit_exactly():
             if A is not None:
                 assert A.shape == (s.rows, s.dim if s.opt == "adagrad" else 1)
                 assert np.all(A == np.float32(0.1))
+            if s.master:
+                M = layer.get_master_rows(t, 0, s.rows)
+                assert np.array_equal(M, ci.init_values(12345, t, np.arange(s.rows), s.dim, -0.05, 0.05, "f32"))
     finally:
         layer.close()
 
@@ -368,3 +372,59 @@ def test_rowwise_adagrad_dims_pooling_and_split_rows(variant):
 
     w, b, g = _custom(tabs, B, lens, keys, seed=8)
     check_step(w, b, g, variant)
+
+
+def _round_stored(m32: np.ndarray, dtype: str) -> np.ndarray:
+    """Nearest-even rounding of fp32 values to the storage type, as binary64
+    (NumPy's fp16 conversion, torch's bf16 conversion)."""
+    import torch
+    if dtype == "f16":
+        return m32.astype(np.float16).astype(np.float64)
+    return torch.from_numpy(np.ascontiguousarray(m32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_master_copy_parity(variant):
+    # 16-bit tables with an fp32 master next to one without: the stored rows
+    # match the oracle's, the masters match the oracle's masters, and every
+    # stored row is its GPU master rounded to nearest-even
+    import torch
+    tabs = [ci.TableSpec(3000, 16, "f16", "sum", "adagrad", 0.01, 1e-8, 0.0, master=True),
+            ci.TableSpec(800, 64, "bf16", "mean", "rowwise_adagrad", 0.02, 1e-8, 0.1, master=True),
+            ci.TableSpec(500, 8, "f16", "sum", "sgd", 0.01),
+            ci.TableSpec(200, 128, "bf16", "sum", "sgd", 0.05, master=True)]
+    B = 1200
+    lens = np.random.default_rng(12).integers(0, 10, size=len(tabs) * B)
+
+    def keys(rng, t, s, L):
+        k = rng.integers(0, s.rows, L)
+        k[rng.random(L) < 0.3] = 5
+        return k
+
+    w, b, g = _custom(tabs, B, lens, keys, seed=13)
+    seed = 0
+    gs = run_gpu_step(w, b, g, variant, seed, keep_layer=True)
+    layer = gs.layer
+    try:
+        assert gs.status_fwd == 0 and gs.status_bwd == 0
+        ref = oracle.step(w.tables, w.batch, b.offsets, b.keys, b.table_ids, g, init_rows_fn(w, seed),
+                          lambda t, r: ci.init_values(seed, t, r, w.tables[t].dim, w.w_lo, w.w_hi, "f32"))
+        assert max_rel_err(gs.out, ref.out, ref.out_scale) <= 1e-5
+        for t, spec in enumerate(w.tables):
+            sel = np.nonzero(ref.rows.table == t)[0]
+            rows = ref.rows.row[sel]
+            idx = ref.rows.row_start[sel][:, None] + np.arange(spec.dim)[None, :]
+            W, A = gather_rows(layer, w, t, rows)
+            assert max_rel_err(W, ref.W[idx], ref.W_scale[idx]) <= TOL[spec.dtype], t
+            if spec.opt != "sgd":
+                ra, rs = ref_state(spec, ref.A, ref.A_scale, idx)
+                assert max_rel_err(A, ra, rs) <= 1e-5, t
+            if spec.master:
+                M = layer.gather_master_rows(t, torch.from_numpy(rows).cuda()).cpu().numpy()
+                assert max_rel_err(M, ref.M[idx], ref.W_scale[idx]) <= 1e-5, t
+                assert np.array_equal(W, _round_stored(M, spec.dtype)), t
+            else:
+                with pytest.raises(Exception):
+                    layer.get_master_rows(t, 0, 1)
+    finally:
+        layer.close()

@@ -159,9 +159,7 @@ __device__ __forceinline__ float group_sum(float v, int width, uint32_t mask)
 // radix sort of (key, u32 value) pairs
 // ---------------------------------------------------------------------------
 constexpr int kSortThreads = 256;
-constexpr int kSortItemsSmall = 12;     // 3072-element tiles for n <= kSmallSortMax
-constexpr int kSortItemsLarge = 8;      // 2048-element tiles above
-constexpr int64_t kSmallSortMax = int64_t(8) << 20;
+constexpr int kSortItems = 12;          // 3072-element tiles
 constexpr int kMaxDigitBits = 10;
 
 struct SortPlan {
@@ -170,8 +168,8 @@ struct SortPlan {
     int digit_bits;      // D
     int passes_max;      // ceil(bits_max / D)
     int64_t tiles_max;
-    size_t desc_bytes;   // look-back descriptors [tiles][2^D] u64
-    size_t aux_bytes;    // histograms [passes][2^D] + tile counters [passes] u32
+    size_t counts_bytes; // per-tile digit counts [2^D][tiles] u32
+    size_t totals_bytes; // digit totals [2^D] u32
 };
 
 SortPlan make_sort_plan(int64_t n_max, int bits_max);
@@ -181,16 +179,15 @@ SortPlan make_sort_plan(int64_t n_max, int bits_max);
 // n_dev ? *n_dev : n_host (n_host bounds the grid).  Only the low
 // bits_dev ? *bits_dev : plan.bits_max bits are sorted; at least one pass
 // always runs.  vals_in == nullptr means value = index.  key_sub (nullable,
-// 64-bit keys only) is subtracted from every input key first.
-// Returns the number of kernels launched, or -1 on a launch error.
-// `desc` (plan.desc_bytes, zeroed once when allocated) and `aux`
-// (plan.aux_bytes) are scratch; a look-back that gives up sets
-// ERRBIT_TIMEOUT in *err.
+// 64-bit keys only) is subtracted from every input key first.  `counts`
+// (plan.counts_bytes) and `totals` (plan.totals_bytes) are scratch that need
+// no initial contents.  Returns the number of kernels launched, or -1 on a
+// launch error.
 template <typename K>
 int radix_sort_pairs(const SortPlan& plan, const K* keys_in, const uint32_t* vals_in,
                      K* keys_out, uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp,
-                     uint64_t* desc, uint32_t* aux, int64_t n_host, const int64_t* n_dev,
-                     const int32_t* bits_dev, const uint64_t* key_sub, int* err, cudaStream_t st);
+                     uint32_t* counts, uint32_t* totals, int64_t n_host, const int64_t* n_dev,
+                     const int32_t* bits_dev, const uint64_t* key_sub, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // run-length encoding of sorted keys (unique / counts / segment offsets)

@@ -29,8 +29,8 @@ struct emb_layer {
     float* bag_scale = nullptr;
     // sort buffers
     uint32_t *sk = nullptr, *sv = nullptr, *tk = nullptr, *tv = nullptr;
-    uint64_t* sort_desc = nullptr;     // look-back descriptors (zeroed at creation)
-    uint32_t* sort_aux = nullptr;      // histograms and tile counters
+    uint32_t* sort_counts = nullptr;   // per-tile digit counts
+    uint32_t* sort_totals = nullptr;   // digit totals
     SortPlan plan_gid{}, plan_inv{}, plan_ukey{};
     // dedup results
     int64_t* num_unique = nullptr;
@@ -226,10 +226,8 @@ unsigned grid_for(int64_t n, int threads, int64_t cap = 16384)
 struct UniqueWs {
     uint64_t *k_tmp, *k_out;
     uint32_t *v_tmp, *v_out;
-    uint64_t* desc;
-    uint32_t* aux;
-    size_t desc_bytes;
-    int* err;
+    uint32_t* counts;
+    uint32_t* totals;
     int32_t* seg;
     void* rle;
     unsigned long long* mm;
@@ -253,10 +251,8 @@ UniqueWs unique_ws_layout(int64_t n, char* base)
     w.k_out = reinterpret_cast<uint64_t*>(take(sizeof(uint64_t) * m));
     w.v_tmp = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t) * m));
     w.v_out = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t) * m));
-    w.desc = reinterpret_cast<uint64_t*>(take(plan.desc_bytes));
-    w.desc_bytes = plan.desc_bytes;
-    w.aux = reinterpret_cast<uint32_t*>(take(plan.aux_bytes));
-    w.err = reinterpret_cast<int*>(take(sizeof(int)));
+    w.counts = reinterpret_cast<uint32_t*>(take(plan.counts_bytes));
+    w.totals = reinterpret_cast<uint32_t*>(take(plan.totals_bytes));
     w.seg = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (m + 1)));
     w.rle = take(rle_scratch_bytes(m));
     w.mm = reinterpret_cast<unsigned long long*>(take(2 * sizeof(unsigned long long)));
@@ -370,10 +366,10 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
     L->plan_gid = make_sort_plan(n, gid_bits);
     L->plan_ukey = make_sort_plan(L->max_unique, gid_bits);
     L->plan_inv = make_sort_plan(n, bits_for((uint64_t)L->max_unique));
-    size_t desc_bytes = L->plan_gid.desc_bytes, aux_bytes = L->plan_gid.aux_bytes;
+    size_t counts_bytes = L->plan_gid.counts_bytes, totals_bytes = L->plan_gid.totals_bytes;
     for (const SortPlan* pl : {&L->plan_inv, &L->plan_ukey}) {
-        if (pl->desc_bytes > desc_bytes) desc_bytes = pl->desc_bytes;
-        if (pl->aux_bytes > aux_bytes) aux_bytes = pl->aux_bytes;
+        if (pl->counts_bytes > counts_bytes) counts_bytes = pl->counts_bytes;
+        if (pl->totals_bytes > totals_bytes) totals_bytes = pl->totals_bytes;
     }
     uint64_t cap = 1024;
     while (cap < 2 * (uint64_t)(L->max_unique > 0 ? L->max_unique : 1)) cap <<= 1;
@@ -383,8 +379,8 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
     ok = ok && dalloc_n(L, &L->d_tables, num_tables) && dalloc_n(L, &L->gid, n) && dalloc_n(L, &L->bag, n) &&
          dalloc_n(L, &L->bag_scale, (int64_t)num_tables * max_batch) && dalloc_n(L, &L->sk, n) &&
          dalloc_n(L, &L->sv, n) && dalloc_n(L, &L->tk, n) && dalloc_n(L, &L->tv, n) &&
-         dalloc(L, reinterpret_cast<void**>(&L->sort_desc), desc_bytes) &&
-         dalloc(L, reinterpret_cast<void**>(&L->sort_aux), aux_bytes) && dalloc_n(L, &L->num_unique, 1) &&
+         dalloc(L, reinterpret_cast<void**>(&L->sort_counts), counts_bytes) &&
+         dalloc(L, reinterpret_cast<void**>(&L->sort_totals), totals_bytes) && dalloc_n(L, &L->num_unique, 1) &&
          dalloc_n(L, &L->seg_off, n + 1) && dalloc_n(L, &L->cnt, n) && dalloc_n(L, &L->inverse, n) &&
          dalloc_n(L, &L->uniq32, n) && dalloc(L, &L->rle_scratch, rle_scratch_bytes(n)) &&
          dalloc_n(L, &L->htable, (int64_t)cap) && dalloc_n(L, &L->slot_rank, (int64_t)cap) &&
@@ -397,7 +393,6 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
         ok = cudaMemcpy(L->d_tables, L->tabs.data(), sizeof(TableDev) * num_tables, cudaMemcpyHostToDevice) ==
                  cudaSuccess &&
              cudaMemset(L->htable, 0xFF, sizeof(uint32_t) * cap) == cudaSuccess &&
-             cudaMemset(L->sort_desc, 0, desc_bytes) == cudaSuccess &&
              cudaMemset(L->err, 0, sizeof(int)) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
         if (!ok) {
             cudaGetLastError();
@@ -454,8 +449,8 @@ static int launch_dedup(emb_layer* L, int32_t variant, int64_t n, cudaStream_t s
     r.key_limit_dev = nullptr;
     r.gid_of_key = nullptr;
     if (variant == EMB_BWD_REDUCTION) {
-        rc = track(L, radix_sort_pairs<uint32_t>(L->plan_gid, L->gid, L->bag, L->sk, L->sv, L->tk, L->tv, L->sort_desc,
-                                                 L->sort_aux, n, nullptr, nullptr, nullptr, L->err, st));
+        rc = track(L, radix_sort_pairs<uint32_t>(L->plan_gid, L->gid, L->bag, L->sk, L->sv, L->tk, L->tv,
+                                                 L->sort_counts, L->sort_totals, n, nullptr, nullptr, nullptr, st));
         if (rc == EMB_OK && L->keep_dedup)
             rc = track(L, rle_sorted<uint32_t>(L->sk, nullptr, n, limit - 1u, nullptr, nullptr, L->uniq32, L->seg_off,
                                                L->cnt, nullptr, L->num_unique, L->rle_scratch, nullptr, st));
@@ -465,7 +460,7 @@ static int launch_dedup(emb_layer* L, int32_t variant, int64_t n, cudaStream_t s
         L->last_sorted_bags = L->sv;
     } else if (variant == EMB_BWD_UNIQUE_SORT) {
         rc = track(L, radix_sort_pairs<uint32_t>(L->plan_gid, L->gid, nullptr, L->sk, L->sv, L->tk, L->tv,
-                                                 L->sort_desc, L->sort_aux, n, nullptr, nullptr, nullptr, L->err, st));
+                                                 L->sort_counts, L->sort_totals, n, nullptr, nullptr, nullptr, st));
         if (rc == EMB_OK)
             rc = track(L, rle_sorted<uint32_t>(L->sk, L->sv, n, limit - 1u, nullptr, nullptr, L->uniq32, L->seg_off,
                                                L->cnt, reinterpret_cast<int32_t*>(L->inverse), L->num_unique,
@@ -482,15 +477,15 @@ static int launch_dedup(emb_layer* L, int32_t variant, int64_t n, cudaStream_t s
         const int64_t umax = n < L->max_unique ? n : L->max_unique;
         if (rc == EMB_OK)
             rc = track(L, radix_sort_pairs<uint32_t>(L->plan_ukey, L->ukey, L->uslot, L->ukey_s, L->uslot_s, L->tk,
-                                                     L->tv, L->sort_desc, L->sort_aux, umax, L->num_unique, nullptr,
-                                                     nullptr, L->err, st));
+                                                     L->tv, L->sort_counts, L->sort_totals, umax, L->num_unique, nullptr,
+                                                     nullptr, st));
         if (rc == EMB_OK)
             rc = track(L, launch_hash_rank_inverse(L->uslot_s, L->num_unique, L->slot_rank, L->bits_dev, L->seg_off,
                                                    slot_of, n, L->inverse, st));
         if (rc == EMB_OK)
             rc = track(L, radix_sort_pairs<uint32_t>(L->plan_inv, L->inverse, L->bag, L->sk, L->sv, L->tk, L->tv,
-                                                     L->sort_desc, L->sort_aux, n, nullptr, L->bits_dev, nullptr,
-                                                     L->err, st));
+                                                     L->sort_counts, L->sort_totals, n, nullptr, L->bits_dev, nullptr,
+                                                     st));
         if (rc == EMB_OK) rc = track(L, launch_seg_from_sorted(L->sk, n, L->num_unique, L->seg_off, L->cnt, st));
         r.skeys = L->sk;
         r.sbags = L->sv;
@@ -700,16 +695,12 @@ int emb_unique(const int64_t* keys, int64_t n, int64_t* unique, int32_t* inverse
         return EMB_OK;
     }
     SortPlan plan = make_sort_plan(n, 64);
-    // the caller's workspace holds anything: clear the look-back descriptors and the error word
-    if (cudaMemsetAsync(w.desc, 0, w.desc_bytes, st) != cudaSuccess ||
-        cudaMemsetAsync(w.err, 0, sizeof(int), st) != cudaSuccess)
-        return EMB_ERR_CUDA;
     if (launch_minmax(keys, n, w.mm, w.key_sub, w.bits, st) < 0) return EMB_ERR_CUDA;
     if (radix_sort_pairs<uint64_t>(plan, reinterpret_cast<const uint64_t*>(keys), nullptr, w.k_out, w.v_out, w.k_tmp,
-                                   w.v_tmp, w.desc, w.aux, n, nullptr, w.bits, w.key_sub, w.err, st) < 0)
+                                   w.v_tmp, w.counts, w.totals, n, nullptr, w.bits, w.key_sub, st) < 0)
         return EMB_ERR_CUDA;
     if (rle_sorted<uint64_t>(w.k_out, w.v_out, n, ~0ull, w.key_sub, unique, nullptr, seg, counts, inverse, num_unique,
-                             w.rle, w.err, st) < 0)
+                             w.rle, nullptr, st) < 0)
         return EMB_ERR_CUDA;
     return EMB_OK;
 }

@@ -4,21 +4,16 @@
 // de recomendacion a escala", section "Integracion del cluster": RB reduces
 // over equal keys, UB dedups the keys first).
 //
-// Small inputs (up to 8 Mi keys) run three kernels per pass over 2048-key
-// tiles: per-tile digit histogram, a scan of each digit's row over tiles, and
-// stable in-tile ranking in shared memory with coalesced runs written to
-// bucket start + tile offset.  Large inputs run one histogram kernel (the
-// digit counts of every pass in one read of the keys), one kernel turning
-// them into bucket starts, then one kernel per pass over 2048-key tiles that
-// ranks in shared memory and finds the tile's offset among earlier tiles by
-// decoupled look-back (tiles are taken in launch order, so every look-back
-// ends; the spin is still capped and reports ERRBIT_TIMEOUT).
-// The element count and the number of significant key bits may live on the
-// device (the unique-based path only learns them there); passes beyond the
-// significant bits return at once, and the buffers are chosen so the last
+// Each pass runs three kernels over 3072-key tiles: a per-tile digit
+// histogram, a scan of each digit's row over tiles, and stable in-tile
+// ranking in shared memory with coalesced runs written to bucket start + tile
+// offset.  No tile waits on another.  (A one-kernel pass whose tiles find
+// their offsets by decoupled look-back measured slower at every size tried:
+// the chain of published prefixes, not the extra read of the keys, set its
+// pace.)  The element count and the number of significant key bits may live
+// on the device (the unique-based path only learns them there); passes beyond
+// the significant bits return at once, and the buffers are chosen so the last
 // active pass always writes the output.
-#include <atomic>
-
 #include "emb_internal.cuh"
 
 namespace emb {
@@ -93,7 +88,7 @@ __device__ __forceinline__ PassCtx pass_ctx(int64_t n_host, const int64_t* n_dev
     return c;
 }
 
-// ---- small inputs: three kernels per pass (histogram per tile, scan, ranking) ----
+// ---- one pass: three kernels (histogram per tile, scan, ranking) ----
 
 constexpr int kDownsweepBlocks = 4;   // resident blocks per SM the ranking kernel's registers are sized for
 
@@ -292,247 +287,6 @@ sort_downsweep(const K* __restrict__ keys_in, const uint32_t* __restrict__ vals_
     }
 }
 
-// ---- large inputs: one kernel per pass with decoupled look-back ----
-
-// Look-back descriptor of (tile, digit): tag (31 bits) | state (2) | count (31).
-// state 1 = the tile's own count is published, 2 = the inclusive prefix over
-// tiles 0..tile is published.  A descriptor whose tag is not this pass's is
-// stale (earlier pass or call) and reads as "not ready".
-__device__ __forceinline__ uint64_t make_desc(uint32_t tag, uint32_t state, uint32_t value)
-{
-    return ((uint64_t)tag << 33) | ((uint64_t)state << 31) | (uint64_t)(value & 0x7FFFFFFFu);
-}
-
-__device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v)
-{
-    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p)
-{
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-constexpr uint32_t kMaxLookbackPolls = 1u << 22;   // a stuck look-back gives up and reports ERRBIT_TIMEOUT
-
-// Digit histograms of every pass in one read of the keys (LSD histograms do
-// not depend on the order the earlier passes leave).
-template <typename K>
-__global__ void __launch_bounds__(kSortThreads)
-sort_histogram(const K* __restrict__ keys, int64_t n_host, const int64_t* n_dev, const int32_t* bits_dev,
-               int bits_max, int D, int passes_max, const uint64_t* key_sub, uint32_t* __restrict__ hist)
-{
-    PassCtx c = pass_ctx(n_host, n_dev, bits_dev, bits_max, D, 0, kSortThreads);
-    if (!c.active) return;
-    extern __shared__ uint32_t sh[];
-    const int nb = 1 << D;
-    const int np = c.npe < passes_max ? c.npe : passes_max;
-    for (int i = threadIdx.x; i < np * nb; i += kSortThreads) sh[i] = 0;
-    __syncthreads();
-    const K sub = key_sub ? (K)(*key_sub) : (K)0;
-    // four independent coalesced loads per thread and round
-    constexpr int kU = 4;
-    const int64_t stride = (int64_t)gridDim.x * kSortThreads;
-    for (int64_t i = (int64_t)blockIdx.x * kSortThreads + threadIdx.x; i < c.n; i += kU * stride) {
-        K k[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) k[u] = i + u * stride < c.n ? (K)(keys[i + u * stride] - sub) : (K)0;
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            if (i + u * stride < c.n)
-                for (int p = 0; p < np; ++p) atomicAdd(&sh[p * nb + (int)((k[u] >> (p * D)) & (K)(nb - 1))], 1u);
-        }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < np * nb; i += kSortThreads)
-        if (sh[i]) atomicAdd(&hist[i], sh[i]);
-}
-
-// Exclusive scan over digits of each pass's histogram, in place: the start
-// of every digit's bucket in the pass's output.
-__global__ void __launch_bounds__(kSortThreads)
-sort_bases(uint32_t* __restrict__ hist, int D)
-{
-    __shared__ uint32_t wbuf[kSortThreads / 32 + 1];
-    uint32_t* h = hist + (size_t)blockIdx.x * (1u << D);
-    const int nb = 1 << D;
-    const int per = (nb + kSortThreads - 1) / kSortThreads;
-    const int d0 = threadIdx.x * per;
-    uint32_t v[4], sum = 0;
-    for (int q = 0; q < per && q < 4; ++q) {
-        v[q] = d0 + q < nb ? h[d0 + q] : 0u;
-        sum += v[q];
-    }
-    uint32_t ex = block_exclusive_sum(sum, wbuf, nullptr);
-    for (int q = 0; q < per && q < 4; ++q) {
-        if (d0 + q < nb) h[d0 + q] = ex;
-        ex += v[q];
-    }
-}
-
-// One LSD pass: tiles taken in launch order from a counter, stable in-tile
-// ranking in shared memory, the tile's position among earlier tiles found by
-// decoupled look-back, then coalesced runs written out.
-template <typename K, int ITEMS>
-__global__ void __launch_bounds__(kSortThreads)
-sort_onesweep(const K* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, K* keys_out, uint32_t* vals_out,
-              K* keys_tmp, uint32_t* vals_tmp, int64_t n_host, const int64_t* n_dev, const int32_t* bits_dev,
-              int bits_max, int D, int pass, const uint64_t* key_sub, const uint32_t* __restrict__ bases,
-              uint64_t* desc, uint32_t* tile_ctr, uint32_t tag, int* err)
-{
-    constexpr int kTile = kSortThreads * ITEMS;
-    constexpr int kWarps = kSortThreads / 32;
-    PassCtx c = pass_ctx(n_host, n_dev, bits_dev, bits_max, D, pass, kTile);
-    if (!c.active) return;
-    const int nb = 1 << D;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    K* skey = reinterpret_cast<K*>(smem_raw);
-    uint32_t* sval = reinterpret_cast<uint32_t*>(skey + kTile);
-    uint32_t* wcnt = sval + kTile;            // [kWarps][nb]
-    uint32_t* tcnt = wcnt + kWarps * nb;      // [nb] tile counts, then tile-local starts
-    uint32_t* gbase = tcnt + nb;              // [nb]
-    uint32_t* wbuf = gbase + nb;              // [kWarps + 2]
-
-    if (threadIdx.x == 0) wbuf[kWarps + 1] = atomicAdd(tile_ctr + pass, 1u);
-    for (int i = threadIdx.x; i < kWarps * nb; i += kSortThreads) wcnt[i] = 0;
-    __syncthreads();
-    const int64_t tile = wbuf[kWarps + 1];
-    if (tile >= c.ntiles) return;
-
-    const K* src_k;
-    const uint32_t* src_v;
-    K* dst_k;
-    uint32_t* dst_v;
-    if (c.dst_out) { dst_k = keys_out; dst_v = vals_out; } else { dst_k = keys_tmp; dst_v = vals_tmp; }
-    if (c.src_in) { src_k = keys_in; src_v = vals_in; }
-    else if (c.dst_out) { src_k = keys_tmp; src_v = vals_tmp; }
-    else { src_k = keys_out; src_v = vals_out; }
-
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int shift = pass * D;
-    const K sub = (c.src_in && key_sub) ? (K)(*key_sub) : (K)0;
-    const int64_t base = tile * kTile;
-    const uint32_t lt = lanemask_lt();
-
-    K k[ITEMS];
-    uint32_t v[ITEMS];
-    uint32_t dg[ITEMS];
-    uint32_t rk[ITEMS];
-#pragma unroll
-    for (int r = 0; r < ITEMS; ++r) {
-        const int e = warp * (ITEMS * 32) + r * 32 + lane;
-        const int64_t idx = base + e;
-        dg[r] = (uint32_t)nb;
-        k[r] = 0;
-        v[r] = 0;
-        if (idx < c.n) {
-            k[r] = (K)(src_k[idx] - sub);
-            v[r] = src_v ? src_v[idx] : (uint32_t)idx;
-            dg[r] = (uint32_t)((k[r] >> shift) & (K)(nb - 1));
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < ITEMS; ++r) {
-        uint32_t peers = __match_any_sync(0xffffffffu, dg[r]);
-        int leader = __ffs(peers) - 1;
-        uint32_t old = 0;
-        if (lane == leader && dg[r] < (uint32_t)nb) {
-            old = wcnt[warp * nb + dg[r]];
-            wcnt[warp * nb + dg[r]] = old + (uint32_t)__popc(peers);
-        }
-        old = __shfl_sync(0xffffffffu, old, leader);
-        rk[r] = old + (uint32_t)__popc(peers & lt);
-        __syncwarp();
-    }
-    __syncthreads();
-    // per digit: exclusive prefix over warps, the tile's count, published at once
-    uint64_t* my_desc = desc + (size_t)tile * nb;
-    for (int d = threadIdx.x; d < nb; d += kSortThreads) {
-        uint32_t s = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            uint32_t cnt = wcnt[w * nb + d];
-            wcnt[w * nb + d] = s;
-            s += cnt;
-        }
-        tcnt[d] = s;
-        st_relaxed(my_desc + d, make_desc(tag, tile == 0 ? 2u : 1u, s));
-    }
-    // decoupled look-back: add earlier tiles' counts until an inclusive prefix is found
-    for (int d = threadIdx.x; d < nb; d += kSortThreads) {
-        uint32_t excl = 0;
-        int64_t t2 = tile - 1;
-        uint32_t polls = 0;
-        while (t2 >= 0) {
-            const uint64_t x = ld_relaxed(desc + (size_t)t2 * nb + d);
-            if ((uint32_t)(x >> 33) != tag) {
-                if (++polls > kMaxLookbackPolls) {
-                    atomicOr(err, ERRBIT_TIMEOUT);
-                    break;
-                }
-                continue;
-            }
-            excl += (uint32_t)(x & 0x7FFFFFFFu);
-            if (((x >> 31) & 3u) == 2u) break;
-            --t2;
-        }
-        if (tile > 0) st_relaxed(my_desc + d, make_desc(tag, 2u, excl + tcnt[d]));
-        gbase[d] = bases[(size_t)pass * nb + d] + excl;
-    }
-    __syncthreads();
-    // tile-local starts: exclusive scan of the tile counts over digits
-    {
-        const int per = (nb + kSortThreads - 1) / kSortThreads;
-        const int d0 = threadIdx.x * per;
-        uint32_t st = 0, lv[4];
-        for (int q = 0; q < per && q < 4; ++q) {
-            lv[q] = (d0 + q < nb) ? tcnt[d0 + q] : 0u;
-            st += lv[q];
-        }
-        uint32_t ex = block_exclusive_sum(st, wbuf, nullptr);
-        for (int q = 0; q < per && q < 4; ++q) {
-            if (d0 + q < nb) tcnt[d0 + q] = ex;
-            ex += lv[q];
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < ITEMS; ++r) {
-        if (dg[r] < (uint32_t)nb) {
-            uint32_t lp = tcnt[dg[r]] + wcnt[warp * nb + dg[r]] + rk[r];
-            skey[lp] = k[r];
-            sval[lp] = v[r];
-        }
-    }
-    __syncthreads();
-    const int64_t rem = c.n - base;
-    const int nvalid = rem < kTile ? (int)rem : kTile;
-#pragma unroll 4
-    for (int r = 0; r < ITEMS; ++r) {
-        const int p = r * kSortThreads + threadIdx.x;
-        if (p < nvalid) {
-            K kk = skey[p];
-            uint32_t d = (uint32_t)((kk >> shift) & (K)(nb - 1));
-            int64_t o = (int64_t)gbase[d] + (p - (int64_t)tcnt[d]);
-            dst_k[o] = kk;
-            dst_v[o] = sval[p];
-        }
-    }
-}
-
-std::atomic<uint32_t> g_sort_tag{0};
-
-uint32_t next_tag()
-{
-    uint32_t t;
-    do {
-        t = (g_sort_tag.fetch_add(1u) + 1u) & 0x7FFFFFFFu;
-    } while (t == 0);
-    return t;
-}
-
 }  // namespace
 
 SortPlan make_sort_plan(int64_t n_max, int bits_max)
@@ -543,17 +297,10 @@ SortPlan make_sort_plan(int64_t n_max, int bits_max)
     p.bits_max = bits_max;
     p.passes_max = (bits_max + kMaxDigitBits - 1) / kMaxDigitBits;
     p.digit_bits = (bits_max + p.passes_max - 1) / p.passes_max;
-    const int64_t small = n_max < kSmallSortMax ? n_max : kSmallSortMax;
-    const int64_t t_small = (small + kSortThreads * kSortItemsSmall - 1) / (kSortThreads * kSortItemsSmall);
-    const int64_t t_large = (n_max + kSortThreads * kSortItemsLarge - 1) / (kSortThreads * kSortItemsLarge);
-    p.tiles_max = t_small > t_large ? t_small : t_large;
+    p.tiles_max = (n_max + kSortThreads * kSortItems - 1) / (kSortThreads * kSortItems);
     if (p.tiles_max < 1) p.tiles_max = 1;
-    // descriptors [tiles][2^D] u64 for large inputs; the small path keeps its
-    // per-tile counts [2^D][tiles] u32 in the same area
-    p.desc_bytes = ((size_t)1 << p.digit_bits) * (size_t)p.tiles_max * sizeof(uint64_t);
-    // histograms [passes][2^D] + tile counters [passes] for large inputs;
-    // digit totals [2^D] for the small path
-    p.aux_bytes = sizeof(uint32_t) * ((size_t)p.passes_max * ((size_t)1 << p.digit_bits) + 64);
+    p.counts_bytes = sizeof(uint32_t) * ((size_t)1 << p.digit_bits) * (size_t)p.tiles_max;
+    p.totals_bytes = sizeof(uint32_t) * ((size_t)1 << p.digit_bits);
     return p;
 }
 
@@ -594,75 +341,23 @@ static int sort_passes_3k(const SortPlan& plan, const K* keys_in, const uint32_t
     return launched;
 }
 
-template <typename K, int ITEMS>
-static size_t onesweep_smem(int D)
-{
-    const int nb = 1 << D;
-    return (size_t)kSortThreads * ITEMS * (sizeof(K) + sizeof(uint32_t)) +
-           sizeof(uint32_t) * ((size_t)(kSortThreads / 32) * nb + 2 * (size_t)nb + kSortThreads / 32 + 2);
-}
-
-template <typename K, int ITEMS>
-static int sort_passes(const SortPlan& plan, const K* keys_in, const uint32_t* vals_in, K* keys_out,
-                       uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp, uint64_t* desc, uint32_t* aux,
-                       int64_t n_host, const int64_t* n_dev, const int32_t* bits_dev, const uint64_t* key_sub,
-                       int* err, cudaStream_t st)
-{
-    constexpr int kTile = kSortThreads * ITEMS;
-    const int D = plan.digit_bits;
-    const int nb = 1 << D;
-    const int64_t tiles = (n_host + kTile - 1) / kTile;
-    uint32_t* hist = aux;                                    // [passes][nb]
-    uint32_t* tile_ctr = aux + (size_t)plan.passes_max * nb; // [passes]
-    if (cudaMemsetAsync(aux, 0, sizeof(uint32_t) * ((size_t)plan.passes_max * nb + plan.passes_max), st) !=
-        cudaSuccess)
-        return -1;
-    const size_t hsmem = sizeof(uint32_t) * (size_t)plan.passes_max * nb;
-    if (cudaFuncSetAttribute(sort_histogram<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem) != cudaSuccess)
-        return -1;
-    int64_t hblocks = (n_host + 4 * kSortThreads * 16 - 1) / (4 * kSortThreads * 16);
-    if (hblocks < 1) hblocks = 1;
-    if (hblocks > 2048) hblocks = 2048;
-    sort_histogram<K><<<(unsigned)hblocks, kSortThreads, hsmem, st>>>(keys_in, n_host, n_dev, bits_dev, plan.bits_max,
-                                                                       D, plan.passes_max, key_sub, hist);
-    sort_bases<<<plan.passes_max, kSortThreads, 0, st>>>(hist, D);
-    const size_t smem = onesweep_smem<K, ITEMS>(D);
-    if (cudaFuncSetAttribute(sort_onesweep<K, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return -1;
-    for (int p = 0; p < plan.passes_max; ++p) {
-        sort_onesweep<K, ITEMS><<<(unsigned)tiles, kSortThreads, smem, st>>>(
-            keys_in, vals_in, keys_out, vals_out, keys_tmp, vals_tmp, n_host, n_dev, bits_dev, plan.bits_max, D, p,
-            key_sub, hist, desc, tile_ctr, next_tag(), err);
-    }
-    if (cudaGetLastError() != cudaSuccess) return -1;
-    return 2 + plan.passes_max;
-}
-
-// Small inputs (at most kSmallSortMax keys, where a look-back would walk long
-// chains of concurrently running tiles) take the three-kernel pass over
-// 2048-key tiles; large ones the one-kernel pass over 2048-key tiles.
 template <typename K>
 int radix_sort_pairs(const SortPlan& plan, const K* keys_in, const uint32_t* vals_in, K* keys_out,
-                     uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp, uint64_t* desc, uint32_t* aux,
-                     int64_t n_host, const int64_t* n_dev, const int32_t* bits_dev, const uint64_t* key_sub, int* err,
+                     uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp, uint32_t* counts, uint32_t* totals,
+                     int64_t n_host, const int64_t* n_dev, const int32_t* bits_dev, const uint64_t* key_sub,
                      cudaStream_t st)
 {
     if (n_host <= 0) return 0;
-    if (n_host <= kSmallSortMax)   // per-tile counts live in the descriptor area, digit totals in aux
-        return sort_passes_3k<K, kSortItemsSmall>(plan, keys_in, vals_in, keys_out, vals_out, keys_tmp, vals_tmp,
-                                                  reinterpret_cast<uint32_t*>(desc), aux, n_host, n_dev, bits_dev,
-                                                  key_sub, st);
-    return sort_passes<K, kSortItemsLarge>(plan, keys_in, vals_in, keys_out, vals_out, keys_tmp, vals_tmp, desc, aux,
-                                           n_host, n_dev, bits_dev, key_sub, err, st);
+    return sort_passes_3k<K, kSortItems>(plan, keys_in, vals_in, keys_out, vals_out, keys_tmp, vals_tmp, counts,
+                                         totals, n_host, n_dev, bits_dev, key_sub, st);
 }
 
 template int radix_sort_pairs<uint32_t>(const SortPlan&, const uint32_t*, const uint32_t*, uint32_t*, uint32_t*,
-                                        uint32_t*, uint32_t*, uint64_t*, uint32_t*, int64_t, const int64_t*,
-                                        const int32_t*, const uint64_t*, int*, cudaStream_t);
+                                        uint32_t*, uint32_t*, uint32_t*, uint32_t*, int64_t, const int64_t*,
+                                        const int32_t*, const uint64_t*, cudaStream_t);
 template int radix_sort_pairs<uint64_t>(const SortPlan&, const uint64_t*, const uint32_t*, uint64_t*, uint32_t*,
-                                        uint64_t*, uint32_t*, uint64_t*, uint32_t*, int64_t, const int64_t*,
-                                        const int32_t*, const uint64_t*, int*, cudaStream_t);
+                                        uint64_t*, uint32_t*, uint32_t*, uint32_t*, int64_t, const int64_t*,
+                                        const int32_t*, const uint64_t*, cudaStream_t);
 
 // ---------------------------------------------------------------------------
 // run-length encoding of sorted keys

@@ -47,7 +47,7 @@ typedef enum {
     EMB_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed */
     EMB_ERR_KEY_RANGE = -4,     /* GPU saw a key outside [0, rows) */
     EMB_ERR_CAPACITY = -5,      /* GPU hash table full */
-    EMB_ERR_TIMEOUT = -6,       /* a bounded GPU wait gave up */
+    EMB_ERR_TIMEOUT = -6,       /* a bounded GPU wait gave up (reserved: no current kernel waits) */
     EMB_ERR_STATE = -7          /* call out of order (e.g. backward before any forward) */
 } emb_status;
 

@@ -36,7 +36,7 @@ import numpy as np
 __all__ = [
     "TableSpec", "Workload", "Batch", "WORKLOADS", "workload",
     "make_batch", "make_grad", "init_values", "stored_to_f64",
-    "splitmix64_at", "zipf_keys",
+    "splitmix64_at", "zipf_keys", "dynamic_key", "init_values_dynamic",
 ]
 
 # purposes for SeedSequence keys
@@ -54,6 +54,13 @@ class TableSpec:
     eps: float = 1e-8
     init_acc: float = 0.0
     master: bool = False        # keep an fp32 master copy (16-bit storage only)
+    dynamic: bool = False       # keys are arbitrary int64 ids; rows is the hash-map capacity
+
+    @property
+    def key_space(self) -> int:
+        """Distinct keys a batch draws from: rows, or half the capacity of a
+        dynamic table (so its map stays at most half full)."""
+        return max(1, self.rows // 2) if self.dynamic else self.rows
 
 
 @dataclasses.dataclass(frozen=True)
@@ -229,11 +236,13 @@ def make_batch(w: Workload, seed: Optional[int] = None) -> Batch:
         lo, hi = int(offsets[t * B]), int(offsets[(t + 1) * B])
         rng = _rng(seed, _P_KEYS, t)
         if w.key_dist == "uniform":
-            keys[lo:hi] = rng.integers(0, spec.rows, size=hi - lo)
+            keys[lo:hi] = rng.integers(0, spec.key_space, size=hi - lo)
         elif w.key_dist == "zipf":
-            keys[lo:hi] = zipf_keys(rng, spec.rows, w.alpha, hi - lo)
+            keys[lo:hi] = zipf_keys(rng, spec.key_space, w.alpha, hi - lo)
         else:
             raise ValueError(w.key_dist)
+        if spec.dynamic:
+            keys[lo:hi] = dynamic_key(t, keys[lo:hi])
     table_ids = np.repeat(np.arange(T, dtype=np.int32), B)
     return Batch(keys=keys, offsets=offsets, table_ids=table_ids, batch=B)
 
@@ -284,6 +293,36 @@ def init_values(seed: int, table: int, rows: np.ndarray, dim: int, lo: float, hi
     d = np.float32(hi) - np.float32(lo)
     w = np.float32(lo) + d * f
     w = w.astype(np.float32)
+    if dtype == "f32":
+        return w
+    if dtype == "f16":
+        return w.astype(np.float16)
+    if dtype == "bf16":
+        return _f32_to_bf16_bits(w)
+    raise ValueError(dtype)
+
+
+def dynamic_key(table: int, rank: np.ndarray) -> np.ndarray:
+    """The int64 id of key rank ``rank`` of a dynamic table: splitmix64 output
+    number rank of the stream seeded with the table index (a bijection of the
+    rank for each table), so ids look like arbitrary 64-bit hashes.  The
+    value -2^63 is reserved (empty map slot) and replaced by 2^63 - 1."""
+    k = splitmix64_at(int(table), np.asarray(rank, dtype=np.uint64)).view(np.int64)
+    return np.where(k == np.iinfo(np.int64).min, np.iinfo(np.int64).max, k)
+
+
+def init_values_dynamic(seed: int, table: int, keys: np.ndarray, dim: int, lo: float, hi: float,
+                        dtype: str = "f32") -> np.ndarray:
+    """Initial values of the rows of keys ``keys`` of a dynamic table, like
+    ``init_values`` but with splitmix64 output number
+    (key << 8) ^ (table << 57) ^ c (64-bit wrap-around) for column c."""
+    k = np.asarray(keys, dtype=np.int64).view(np.uint64).reshape(-1, 1)
+    cols = np.arange(dim, dtype=np.uint64).reshape(1, -1)
+    with np.errstate(over="ignore"):
+        n = (k << np.uint64(8)) ^ (np.uint64(table) << np.uint64(57)) ^ cols
+    h = splitmix64_at(seed, n)
+    f = (h >> np.uint64(40)).astype(np.float32) * np.float32(2.0 ** -24)
+    w = (np.float32(lo) + (np.float32(hi) - np.float32(lo)) * f).astype(np.float32)
     if dtype == "f32":
         return w
     if dtype == "f16":

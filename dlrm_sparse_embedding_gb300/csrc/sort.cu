@@ -111,11 +111,16 @@ sort_upsweep(const K* __restrict__ keys_in, const K* keys_out, const K* keys_tmp
     const K sub = (c.src_in && key_sub) ? (K)(*key_sub) : (K)0;
     const int64_t base = tile * kTile;
     const int lane = threadIdx.x & 31;
-#pragma unroll 4
+    // all of the thread's keys are requested before the first is counted
+    uint32_t dg[ITEMS];
+#pragma unroll
     for (int r = 0; r < ITEMS; ++r) {
-        int64_t idx = base + (int64_t)r * kSortThreads + threadIdx.x;
-        uint32_t d = (uint32_t)nb;
-        if (idx < c.n) d = (uint32_t)(((K)(src[idx] - sub) >> shift) & (K)(nb - 1));
+        const int64_t idx = base + (int64_t)r * kSortThreads + threadIdx.x;
+        dg[r] = idx < c.n ? (uint32_t)(((K)(src[idx] - sub) >> shift) & (K)(nb - 1)) : (uint32_t)nb;
+    }
+#pragma unroll
+    for (int r = 0; r < ITEMS; ++r) {
+        const uint32_t d = dg[r];
         uint32_t peers = __match_any_sync(0xffffffffu, d);
         int leader = __ffs(peers) - 1;
         if (lane == leader && d < (uint32_t)nb) atomicAdd(&hist[d], (uint32_t)__popc(peers));

@@ -336,3 +336,38 @@ def step(tables, B: int, offsets, keys, table_ids, grad_out,
     G, Gabs = reduce(tables, B, offsets, inv, rows, grad_out)
     M, A, Ws, As, W = update(tables, upd_rows, state, G, Gabs)
     return StepResult(gids, bad, uniq, inv, cnt, seg, out, oscale, rows, W, M, A, Ws, As, G, Gabs)
+
+
+def step_dynamic(tables, B: int, offsets, keys, table_ids, grad_out,
+                 init_rows: Callable[[int, np.ndarray], np.ndarray],
+                 init_dynamic: Callable[[int, np.ndarray], np.ndarray],
+                 init_master: Optional[Callable[[int, np.ndarray], np.ndarray]] = None,
+                 init_dynamic_master: Optional[Callable[[int, np.ndarray], np.ndarray]] = None):
+    """A step on a layer with dynamic tables (``dynamic`` set): such a table
+    maps arbitrary int64 keys to rows, each row starting at
+    init_dynamic(t, keys) when its key first appears.  By that definition it
+    is a table over its distinct keys, so each dynamic table's keys are
+    relabelled to dense ids (ascending key order; the reserved key -2^63 is
+    skipped like an out-of-range key) and the plain step runs on the result.
+    Returns (StepResult, key_of) with key_of[t] the keys of table t's dense
+    ids (dynamic tables only)."""
+    keys2 = np.array(keys, dtype=np.int64, copy=True)
+    tables2 = list(tables)
+    key_of = {}
+    for t, spec in enumerate(tables):
+        if not getattr(spec, "dynamic", False):
+            continue
+        lo, hi = int(offsets[t * B]), int(offsets[(t + 1) * B])
+        k = keys2[lo:hi]
+        valid = k != np.iinfo(np.int64).min
+        uk, inv = np.unique(k[valid], return_inverse=True)
+        dense = np.full(hi - lo, -1, dtype=np.int64)
+        dense[valid] = inv
+        keys2[lo:hi] = dense
+        tables2[t] = dataclasses.replace(spec, rows=max(int(uk.size), 1), dynamic=False)
+        key_of[t] = uk
+    rows_fn = lambda t, r: init_dynamic(t, key_of[t][r]) if t in key_of else init_rows(t, r)
+    master_fn = None
+    if init_master is not None or init_dynamic_master is not None:
+        master_fn = lambda t, r: (init_dynamic_master(t, key_of[t][r]) if t in key_of else init_master(t, r))
+    return step(tables2, B, offsets, keys2, table_ids, grad_out, rows_fn, master_fn), key_of

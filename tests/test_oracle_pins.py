@@ -492,6 +492,35 @@ def test_master_copy_keeps_a_step_below_half_a_16bit_ulp():
     assert mast.M.tolist() == [0.999755859375] * 4 + [0.99951171875] * 4
 
 
+def test_dynamic_table_is_the_static_table_over_its_keys():
+    # a dynamic table over scrambled 64-bit ids gives exactly the static
+    # table's step over the ranks, row for row (each id's row starts at the
+    # value the static table's row for its rank starts at)
+    B, rows, dim = 300, 64, 8
+    offsets, keys, tid = _random_csr(2, B, [rows, rows], 5, 61)
+    rng = np.random.default_rng(62)
+    grad = rng.standard_normal((B, 2 * dim)).astype(np.float32)
+    ids = {t: ci.dynamic_key(t, np.arange(rows)) for t in range(2)}
+    keys_dyn = keys.copy()
+    lo = offsets[B]
+    keys_dyn[lo:] = ids[1][keys[lo:]]                       # table 1 dynamic, table 0 static
+    W0 = [rng.uniform(-0.05, 0.05, (rows, dim)).astype(np.float32) for _ in range(2)]
+    static = [_spec(rows, dim, "sum", "adagrad"), _spec(rows, dim, "mean", "rowwise_adagrad")]
+    ref = oracle.step(static, B, offsets, keys, tid, grad, _dense_rows(W0))
+    rank_of = {int(k): r for r, k in enumerate(ids[1])}
+    dyn_specs = [static[0], ci.TableSpec(2 * rows, dim, "f32", "mean", "rowwise_adagrad", 0.01, 1e-8, dynamic=True)]
+    res, key_of = oracle.step_dynamic(dyn_specs, B, offsets, keys_dyn, tid, grad, _dense_rows(W0),
+                                      lambda t, k: W0[t][[rank_of[int(x)] for x in k]])
+    assert np.array_equal(res.out, ref.out)
+    for k in range(res.unique.shape[0]):
+        t, r = int(res.rows.table[k]), int(res.rows.row[k])
+        rank = r if t == 0 else rank_of[int(key_of[1][r])]
+        kr = int(np.nonzero((ref.rows.table == t) & (ref.rows.row == rank))[0][0])
+        a, b = res.rows.row_start[k], ref.rows.row_start[kr]
+        assert np.array_equal(res.W[a:a + dim], ref.W[b:b + dim])
+        assert np.array_equal(res.A[a:a + dim], ref.A[b:b + dim])
+
+
 def _torch_reference_step(tables, B, offsets, keys, grad, W, opt_name):
     """Independent reference: torch embedding_bag (float64, sparse grads) + torch.optim."""
     outs, params = [], []

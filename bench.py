@@ -47,6 +47,9 @@ CONFIG_TEXT = {
              "hotness 20, Zipf(1.1), sum pooling"),
     "huge_master": ("single huge table with an fp32 master copy: 1 fp16 table x 2e8 rows x dim 64 plus fp32 master "
                     "and fp32 Adagrad state, batch 131,072, hotness 20, Zipf(1.1), sum pooling"),
+    "dlrm_dynamic": ("DLRM-style one-hot with dynamic tables: 26 fp32 tables of int64 ids (scrambled Zipf(1.05) "
+                     "ranks, key spaces log-uniform in [1e3,1e7]) behind GPU hash maps of twice that many rows, "
+                     "dim 128, batch 65,536, hotness 1, sum pooling, Adagrad"),
     "dlrm_rowwise": ("DLRM-style one-hot with row-wise Adagrad: 26 fp32 tables, rows log-uniform in [1e3,1e7], "
                      "dim 128, batch 65,536, hotness 1, Zipf(1.05) keys, sum pooling, one fp32 accumulator per row"),
     "skew": ("skewed dedup stress: 8 fp32 tables dims {16,32,64,128}x2 x 5e6 rows, batch 262,144, hotness 50, "
@@ -80,6 +83,10 @@ def algorithmic_bytes(w: ci.Workload, batch: ci.Batch, U_per_table: np.ndarray) 
     state_bytes = sum(int(U_per_table[t]) * 4 * (s.dim if state_cols[s.opt] is None else state_cols[s.opt])
                       for t, s in enumerate(w.tables))
     fwd = 8 * nnz + 8 * (T * B + 1) + 4 * T * B + rows_bytes + 4 * B * D + 8 * nnz   # + gid/bag ids written
+    # dynamic tables: each lookup also reads its map slot and writes and re-reads its resolved row
+    dyn_lookups = sum(int(batch.offsets[(t + 1) * B] - batch.offsets[t * B])
+                      for t, s in enumerate(w.tables) if getattr(s, "dynamic", False))
+    fwd += 24 * dyn_lookups
     dedup = 8 * nnz + 8 * nnz                                    # read (id, bag) pairs, write them sorted
     upd = 4 * B * D + 8 * nnz + 2 * rows_bytes + 2 * state_bytes + master_bytes   # grad once, sorted ids+bags, row/state r+w
     return {"forward": fwd, "dedup": dedup, "reduce_update": upd, "step": fwd + dedup + upd}
@@ -176,6 +183,14 @@ def _dist():
 def oracle_step_timed(w: ci.Workload, batch: ci.Batch, grad: np.ndarray, seed: int) -> float:
     """Seconds the CPU oracle takes for a1..a5 on `batch` (initial rows prepared untimed)."""
     import oracle
+    if any(getattr(s, "dynamic", False) for s in w.tables):
+        # dynamic tables: the oracle relabels keys to rows and prepares the rows inside the timed step
+        t0 = time.perf_counter()
+        oracle.step_dynamic(
+            w.tables, w.batch, batch.offsets, batch.keys, batch.table_ids, grad,
+            lambda t, r: ci.init_values(seed, t, r, w.tables[t].dim, w.w_lo, w.w_hi, w.tables[t].dtype),
+            lambda t, k: ci.init_values_dynamic(seed, t, k, w.tables[t].dim, w.w_lo, w.w_hi, w.tables[t].dtype))
+        return time.perf_counter() - t0
     gids, _ = oracle.global_ids(w.tables, w.batch, batch.offsets, batch.keys, batch.table_ids)
     u, inv, _, _ = oracle.unique(gids, skip_negative=True)
     rows = oracle.make_row_store(w.tables, u, lambda t, r: ci.init_values(

@@ -155,6 +155,11 @@ def _build_workloads() -> dict:
         batch=262144, hot_kind="fixed", hot_lo=50, hot_hi=50, key_dist="zipf", alpha=1.5)
     # the dlrm workload with one Adagrad accumulator per row instead of per element
     w["dlrm_rowwise"] = w["dlrm"].replace(name="dlrm_rowwise").with_tables(opt="rowwise_adagrad")
+    # the dlrm workload with its tables behind hash maps: the same Zipf ranks,
+    # drawn from the same key spaces, become scrambled int64 ids; each map has
+    # twice as many rows as its key space
+    w["dlrm_dynamic"] = w["dlrm"].replace(name="dlrm_dynamic", tables=tuple(
+        dataclasses.replace(t, rows=2 * t.rows, dynamic=True) for t in w["dlrm"].tables))
     # the huge fp16 table with an fp32 master copy
     w["huge_master"] = w["huge"].replace(name="huge_master").with_tables(master=True)
     return w

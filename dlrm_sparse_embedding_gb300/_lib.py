@@ -31,7 +31,7 @@ EXPORTS = (
     "emb_set_keep_dedup", "emb_dedup_result", "emb_unique_workspace", "emb_unique",
     "emb_get_rows", "emb_set_rows", "emb_gather_rows", "emb_sync_status", "emb_launch_count",
     "emb_set_timing", "emb_phase_times", "emb_unique_noalloc", "emb_set_early_dedup",
-    "emb_get_master_rows", "emb_set_master_rows", "emb_gather_master_rows", "emb_status_string",
+    "emb_get_master_rows", "emb_set_master_rows", "emb_gather_master_rows", "emb_find_keys", "emb_status_string",
 )
 UNIQUE_NOALLOC_MAX_KEYS = 262144
 PHASES = ("forward", "dedup", "reduce_update")
@@ -40,7 +40,8 @@ PHASES = ("forward", "dedup", "reduce_update")
 class EmbTableSpec(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int64), ("dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("pooling", ctypes.c_int32), ("opt", ctypes.c_int32), ("lr", ctypes.c_float),
-                ("eps", ctypes.c_float), ("init_acc", ctypes.c_float), ("master_fp32", ctypes.c_int32)]
+                ("eps", ctypes.c_float), ("init_acc", ctypes.c_float), ("master_fp32", ctypes.c_int32),
+                ("dynamic", ctypes.c_int32)]
 
 
 class EmbError(RuntimeError):
@@ -79,6 +80,7 @@ def _load() -> ctypes.CDLL:
     L.emb_get_master_rows.argtypes = [vp, i32, i64, i64, vp, vp]
     L.emb_set_master_rows.argtypes = [vp, i32, i64, i64, vp, vp]
     L.emb_gather_master_rows.argtypes = [vp, i32, vp, i64, vp, vp]
+    L.emb_find_keys.argtypes = [vp, i32, vp, i64, vp, vp]
     L.emb_sync_status.argtypes = [vp, vp]
     L.emb_launch_count.argtypes = [vp, ctypes.POINTER(i64), i32]
     L.emb_set_timing.argtypes = [vp, i32]

@@ -39,7 +39,8 @@ struct TableDev {
     int32_t opt;         // emb_opt
     float lr, eps;
     int32_t doff;        // column offset in the concatenated output
-    int32_t pad_;
+    int32_t dynamic;     // 1: keys are int64 ids mapped to rows by map_keys
+    unsigned long long* map_keys;   // dynamic tables: [rows] key held by each row (kMapEmpty = free)
 };
 
 // ---------------------------------------------------------------------------
@@ -252,10 +253,39 @@ struct FwdArgs {
     int64_t warps_per_table;
     bool write_ids;             // the pooling kernel also writes gid_out / bag_out
     bool rows16;                // every table stores 16-bit rows (selects the pooling kernel's occupancy)
+    const int64_t* resolved;    // dynamic tables: row of each lookup (-1: none), read instead of keys
     int* err;
 };
 
 int launch_forward(const FwdArgs& a, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// dynamic tables: int64 keys -> rows through an open-addressing map (dynamic.cu)
+// ---------------------------------------------------------------------------
+constexpr unsigned long long kMapEmpty = 0x8000000000000000ull;   // the reserved key -2^63
+
+struct DynArgs {
+    const int64_t* keys;
+    const int64_t* offsets;
+    int32_t batch;
+    const TableDev* tables;
+    const int32_t* dyn_tables;  // [num_dyn] indices of the dynamic tables
+    int32_t num_dyn;
+    const float* init_acc;      // [T] initial accumulator values
+    uint64_t seed;              // initial values of inserted rows (counter-based, as emb_init_uniform)
+    float lo, hi;
+    int64_t* resolved;          // [nnz] row of each lookup of a dynamic table (-1: reserved key or map full)
+    int* err;
+};
+
+// Finds or inserts the key of every lookup of the dynamic tables; a row taken
+// for a new key gets its initial values.  Returns kernels launched or -1.
+int launch_dyn_resolve(const DynArgs& a, int64_t nnz, cudaStream_t st);
+// Rows of n keys of dynamic table t (-1 when absent), without inserting.
+int launch_dyn_find(const TableDev* tables, int t, const int64_t* keys, int64_t n, int64_t* rows_out,
+                    cudaStream_t st);
+// Marks every row of a map free.
+int launch_dyn_clear(unsigned long long* map_keys, int64_t rows, cudaStream_t st);
 int launch_forward_ids(const FwdArgs& a, cudaStream_t st);   // gid_out / bag_out only
 
 // dedup helpers (dedup.cu); each returns kernels launched or -1

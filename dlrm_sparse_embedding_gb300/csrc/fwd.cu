@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
     if (t >= a.num_tables) return;
     const int64_t B = a.batch;
     const TableDev tb = a.tables[t];
+    const int64_t* kp = tb.dynamic ? a.resolved : a.keys;   // a dynamic table's keys are resolved to rows
     int Lr = 1;
     while (Lr < ((tb.dim + 3) >> 2)) Lr <<= 1;
     const int li = lane & (Lr - 1), g = lane / Lr;
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
         // its pooled value is the row itself, so rows go straight to the output
         const int64_t i = K0 + li;
         const bool in = li < nbg;
-        const int64_t key = in ? __ldg(a.keys + i) : 0;
+        const int64_t key = in ? __ldg(kp + i) : 0;
         const bool valid = in && my_tid_ok && key >= 0 && key < tb.rows;
         if (valid) prefetch_row_l2(tb, key);
         if (in) {
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
     for (int64_t base = K0; base < K1; base += Lr) {
         const int64_t i = base + li;
         const bool in = i < K1;
-        const int64_t key = in ? __ldg(a.keys + i) : 0;
+        const int64_t key = in ? __ldg(kp + i) : 0;
         // bag of position i = number of the group's bags that end at or before i
         int k = 0;
         for (int stp = Lr >> 1; stp > 0; stp >>= 1) {
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(kThreads) fwd_ids(FwdArgs a)
     const int64_t j0 = (int64_t)t * B + bg0;
     const int64_t rows = a.tables[t].rows;
     const uint32_t row_base = a.tables[t].row_base;
+    const int64_t* kp = a.tables[t].dynamic ? a.resolved : a.keys;
     const int64_t K0 = __ldg(a.offsets + j0);
     int64_t my_end = INT64_MAX;
     bool my_tid_ok = true;
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(kThreads) fwd_ids(FwdArgs a)
         }
         const bool tok = __shfl_sync(0xffffffffu, my_tid_ok, k);
         if (i < K1) {
-            const int64_t key = __ldg(a.keys + i);
+            const int64_t key = __ldg(kp + i);
             const bool valid = tok && key >= 0 && key < rows;
             a.gid_out[i] = valid ? row_base + (uint32_t)key : a.sentinel;
             a.bag_out[i] = (uint32_t)(j0 + k);

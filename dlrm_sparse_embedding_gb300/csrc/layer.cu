@@ -53,6 +53,13 @@ struct emb_layer {
     int64_t nchunks_max = 0;
     int* err = nullptr;
     int64_t* scratch64 = nullptr;   // [2]: num-unique copy target, misc
+    // dynamic tables (dynamic.cu)
+    int32_t num_dyn = 0;
+    int32_t* d_dyn_tables = nullptr;  // [num_dyn]
+    float* d_init_acc = nullptr;      // [T]
+    int64_t* resolved = nullptr;      // [max_nnz] row of each lookup of a dynamic table
+    uint64_t dyn_seed = 0;            // initial values of rows inserted later (last emb_init_uniform)
+    float dyn_lo = 0.f, dyn_hi = 0.f;
 
     std::vector<void*> allocs;
     size_t alloc_bytes = 0;
@@ -315,7 +322,7 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
         const emb_table_spec& s = specs[t];
         if (s.rows < 1 || s.dim < 4 || s.dim > kMaxDim || (s.dim & 3) || s.dtype < 0 || s.dtype > 2 ||
             s.pooling < 0 || s.pooling > 1 || s.opt < 0 || s.opt > 2 || s.master_fp32 < 0 || s.master_fp32 > 1 ||
-            (s.master_fp32 && s.dtype == EMB_F32))
+            (s.master_fp32 && s.dtype == EMB_F32) || s.dynamic < 0 || s.dynamic > 1)
             return EMB_ERR_INVALID_ARG;
         total_rows += (uint64_t)s.rows;
         total_dim += s.dim;
@@ -350,13 +357,15 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
         d.lr = s.lr;
         d.eps = s.eps;
         d.doff = doff;
-        d.pad_ = 0;
+        d.dynamic = s.dynamic;
+        d.map_keys = nullptr;
         d.w = nullptr;
         d.state = nullptr;
         d.master = nullptr;
         ok = dalloc(L, &d.w, (size_t)s.rows * s.dim * dtype_bytes(s.dtype));
         if (ok && state_cols(d) > 0) ok = dalloc_n(L, &d.state, s.rows * state_cols(d));
         if (ok && s.master_fp32) ok = dalloc_n(L, &d.master, s.rows * (int64_t)s.dim);
+        if (ok && s.dynamic) ok = dalloc_n(L, &d.map_keys, s.rows);
         rb += (uint64_t)s.rows;
         doff += s.dim;
     }
@@ -388,12 +397,28 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
          dalloc_n(L, &L->ukey_s, L->max_unique) && dalloc_n(L, &L->uslot_s, L->max_unique) &&
          dalloc_n(L, &L->bits_dev, 1) && dalloc_n(L, &L->slots, L->nchunks_max * 2 * kMaxDim) &&
          dalloc_n(L, &L->split_list, L->nchunks_max) && dalloc_n(L, &L->split_count, 1) &&
-         dalloc_n(L, &L->err, 1) && dalloc_n(L, &L->scratch64, 2);
+         dalloc_n(L, &L->err, 1) && dalloc_n(L, &L->scratch64, 2) && dalloc_n(L, &L->d_init_acc, num_tables);
+    std::vector<int32_t> dyn;
+    std::vector<float> init_acc(num_tables);
+    for (int t = 0; t < num_tables; ++t) {
+        if (specs[t].dynamic) dyn.push_back(t);
+        init_acc[t] = specs[t].init_acc;
+    }
+    L->num_dyn = (int32_t)dyn.size();
+    if (ok && L->num_dyn > 0)
+        ok = dalloc_n(L, &L->d_dyn_tables, L->num_dyn) && dalloc_n(L, &L->resolved, n);
     if (ok) {
         ok = cudaMemcpy(L->d_tables, L->tabs.data(), sizeof(TableDev) * num_tables, cudaMemcpyHostToDevice) ==
                  cudaSuccess &&
              cudaMemset(L->htable, 0xFF, sizeof(uint32_t) * cap) == cudaSuccess &&
-             cudaMemset(L->err, 0, sizeof(int)) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
+             cudaMemset(L->err, 0, sizeof(int)) == cudaSuccess &&
+             cudaMemcpy(L->d_init_acc, init_acc.data(), sizeof(float) * num_tables, cudaMemcpyHostToDevice) ==
+                 cudaSuccess &&
+             (L->num_dyn == 0 || cudaMemcpy(L->d_dyn_tables, dyn.data(), sizeof(int32_t) * L->num_dyn,
+                                            cudaMemcpyHostToDevice) == cudaSuccess);
+        for (int t = 0; t < num_tables && ok; ++t)
+            if (L->tabs[t].dynamic) ok = launch_dyn_clear(L->tabs[t].map_keys, L->tabs[t].rows, 0) >= 0;
+        ok = ok && cudaDeviceSynchronize() == cudaSuccess;
         if (!ok) {
             cudaGetLastError();
             free_all(L);
@@ -427,8 +452,16 @@ int emb_destroy(emb_layer* L)
 int emb_init_uniform(emb_layer* L, uint64_t seed, float lo, float hi, void* stream)
 {
     if (!L) return EMB_ERR_INVALID_ARG;
+    L->dyn_seed = seed;
+    L->dyn_lo = lo;
+    L->dyn_hi = hi;
     for (int t = 0; t < L->T; ++t) {
         const TableDev& d = L->tabs[t];
+        if (d.dynamic) {   // rows get their values when a key first takes them
+            if (launch_dyn_clear(d.map_keys, d.rows, S(stream)) < 0) return EMB_ERR_CUDA;
+            L->launches += 1;
+            continue;
+        }
         const int64_t total = d.rows * d.dim;
         init_uniform_kernel<<<grid_for(total, 256, 65536), 256, 0, S(stream)>>>(
             d.w, d.dtype, d.rows, d.dim, t, seed, lo, hi, d.state, (int)state_cols(d), L->specs[t].init_acc,
@@ -520,10 +553,30 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
     a.warps_per_table = (batch + 31) / 32;
     a.write_ids = true;
     a.rows16 = true;
+    a.resolved = L->resolved;
     for (const TableDev& d : L->tabs) a.rows16 = a.rows16 && d.dtype != EMB_F32;
     a.err = L->err;
     if (L->timing) harvest_timing(L);
     int rc = EMB_OK;
+    if (L->timing) cudaEventRecord(L->ev[0], st);   // the forward phase includes resolving dynamic keys
+    if (L->num_dyn > 0 && nnz > 0) {
+        // dynamic tables: find or insert every key; the kernels after it read rows
+        DynArgs da;
+        da.keys = keys;
+        da.offsets = offsets;
+        da.batch = batch;
+        da.tables = L->d_tables;
+        da.dyn_tables = L->d_dyn_tables;
+        da.num_dyn = L->num_dyn;
+        da.init_acc = L->d_init_acc;
+        da.seed = L->dyn_seed;
+        da.lo = L->dyn_lo;
+        da.hi = L->dyn_hi;
+        da.resolved = L->resolved;
+        da.err = L->err;
+        rc = track(L, launch_dyn_resolve(da, nnz, st));
+        if (rc != EMB_OK) return rc;
+    }
     const bool early = L->early_variant >= 0 && nnz > 0;
     if (early) {
         // ids + dedup on the side stream, concurrent with the pooling kernel
@@ -538,7 +591,6 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
         if (rc == EMB_OK && cudaEventRecord(L->ev_ready, L->side) != cudaSuccess) rc = EMB_ERR_CUDA;
         if (rc != EMB_OK) return rc;
     }
-    if (L->timing) cudaEventRecord(L->ev[0], st);
     rc = track(L, launch_forward(a, st));
     if (L->timing && rc == EMB_OK) {
         cudaEventRecord(L->ev[1], st);
@@ -739,6 +791,13 @@ int emb_set_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, const void* w
                              cudaMemcpyHostToDevice, st) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
     return ok ? EMB_OK : EMB_ERR_CUDA;
+}
+
+int emb_find_keys(emb_layer* L, int32_t t, const int64_t* keys, int64_t n, int64_t* rows_out, void* stream)
+{
+    if (!L || t < 0 || t >= L->T || n < 0 || (n > 0 && (!keys || !rows_out)) || !L->tabs[t].dynamic)
+        return EMB_ERR_INVALID_ARG;
+    return track(L, launch_dyn_find(L->d_tables, t, keys, n, rows_out, S(stream)));
 }
 
 int emb_get_master_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, float* master_host, void* stream)

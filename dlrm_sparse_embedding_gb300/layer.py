@@ -49,7 +49,8 @@ class EmbeddingLayer:
     ``tables``: sequence of objects with ``rows, dim`` and optionally
     ``dtype`` ("f32"/"f16"/"bf16"), ``pooling`` ("sum"/"mean"), ``opt``
     ("sgd"/"adagrad"/"rowwise_adagrad"), ``lr``, ``eps``, ``init_acc``,
-    ``master`` (keep an fp32 master copy of a 16-bit table).
+    ``master`` (keep an fp32 master copy of a 16-bit table), ``dynamic``
+    (arbitrary int64 keys mapped to rows by a hash map of ``rows`` slots).
     """
 
     def __init__(self, tables: Sequence, max_batch: int, max_nnz: int):
@@ -66,6 +67,7 @@ class EmbeddingLayer:
             arr[i].eps = float(_spec_field(s, "eps", 1e-8))
             arr[i].init_acc = float(_spec_field(s, "init_acc", 0.0))
             arr[i].master_fp32 = 1 if _spec_field(s, "master", False) else 0
+            arr[i].dynamic = 1 if _spec_field(s, "dynamic", False) else 0
         h = ctypes.c_void_p()
         check(lib.emb_create(arr, T, int(max_batch), int(max_nnz), ctypes.byref(h)), "emb_create")
         self._h = h
@@ -168,6 +170,14 @@ class EmbeddingLayer:
         check(lib.emb_set_rows(self._h, t, row0, w.shape[0], w.ctypes.data_as(ctypes.c_void_p),
                                None if s is None else s.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
               "emb_set_rows")
+
+    # -- dynamic tables -----------------------------------------------------------
+    def find_keys(self, t: int, keys: torch.Tensor, stream=None) -> torch.Tensor:
+        """Rows (int64, -1 when absent) of int64 keys of dynamic table t; inserts nothing."""
+        out = torch.empty(int(keys.numel()), dtype=torch.int64, device=keys.device)
+        check(lib.emb_find_keys(self._h, t, _ptr(keys), int(keys.numel()), _ptr(out), _stream(stream)),
+              "emb_find_keys")
+        return out
 
     # -- fp32 master copies of 16-bit tables ------------------------------------
     def gather_master_rows(self, t: int, rows: torch.Tensor, stream=None) -> torch.Tensor:

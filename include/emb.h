@@ -75,7 +75,18 @@ typedef enum {
  * converted from them.  The layer then holds rows*dim fp32 master values;
  * every update steps the master in fp32 and stores the 16-bit weight as the
  * new master rounded to nearest-even, so steps smaller than half a 16-bit
- * ulp accumulate instead of being rounded away. */
+ * ulp accumulate instead of being rounded away.
+ * dynamic (GTC 2022 HugeCTR slides, "HUGECTR EMBEDDING LAYER": embeddings
+ * behind a GPU hash table): the table's keys are arbitrary int64 ids, not row
+ * indices, and `rows` is the capacity.  emb_forward finds each key's row in an
+ * open-addressing map over the rows (linear probing from a hash of table and
+ * key) and, for a key it has not seen, takes a free row and gives it initial
+ * values: the counter-based values of emb_init_uniform with splitmix64
+ * output number (key << 8) ^ (t << 57) ^ c, the table's init_acc and, with
+ * master_fp32, the fp32 value as master.  Nothing is evicted: a lookup that
+ * finds the table full is skipped and reported as EMB_ERR_CAPACITY.  The key
+ * -2^63 is reserved and reported like an out-of-range key.  Everything after
+ * the lookup (dedup ids, row I/O) uses the row, which emb_find_keys gives. */
 typedef struct {
     int64_t rows;
     int32_t dim;
@@ -86,6 +97,7 @@ typedef struct {
     float eps;
     float init_acc;
     int32_t master_fp32; /* 1: keep an fp32 master copy of a 16-bit table (see below); 0: none */
+    int32_t dynamic;     /* 1: keys are arbitrary int64 ids mapped to rows by a hash map (see below) */
 } emb_table_spec;
 
 typedef struct emb_layer emb_layer;   /* opaque; owns tables, optimizer state and workspace */
@@ -108,7 +120,10 @@ int emb_destroy(emb_layer* layer);
  *   number n = t*2^44 + r*2^12 + c of the stream started from state `seed`,
  * evaluated in fp32 with one rounding per operation and then rounded to
  * nearest-even into the table dtype; set every Adagrad accumulator to its
- * table's init_acc.  Asynchronous on `stream`. */
+ * table's init_acc and every fp32 master to the fp32 value.  A dynamic table
+ * is emptied instead (all keys forgotten); its rows get the same kind of
+ * values, from this seed/lo/hi, when keys take them.  Asynchronous on
+ * `stream`. */
 int emb_init_uniform(emb_layer* layer, uint64_t seed, float lo, float hi, void* stream);
 
 /* Forward: lookup + pooling + concatenation (GTC 2022 HugeCTR slides, "COMMON
@@ -228,6 +243,12 @@ int emb_get_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n, void* wei
                  float* state_host, void* stream);
 int emb_set_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n,
                  const void* weights_host, const float* state_host, void* stream);
+
+/* Rows of n keys (device int64) of dynamic table t, into rows_out (device
+ * int64; -1 for a key the table does not hold).  Inserts nothing.
+ * Asynchronous; EMB_ERR_INVALID_ARG for a table that is not dynamic. */
+int emb_find_keys(emb_layer* layer, int32_t t, const int64_t* keys, int64_t n, int64_t* rows_out,
+                  void* stream);
 
 /* The fp32 master copy of rows [row0, row0+n) of table t (a table created
  * with master_fp32 = 1; EMB_ERR_INVALID_ARG otherwise), n*dim fp32 in host

@@ -428,3 +428,128 @@ def test_master_copy_parity(variant):
                     layer.get_master_rows(t, 0, 1)
     finally:
         layer.close()
+
+
+# ---------------------------------------------------------------------------
+# dynamic tables (int64 keys behind a GPU hash map)
+# ---------------------------------------------------------------------------
+
+def _dynamic_inputs(B=900, seed=21):
+    tabs = [ci.TableSpec(1000, 16, "f32", "sum", "adagrad", 0.01, 1e-8, 0.0),
+            ci.TableSpec(4096, 32, "f32", "mean", "rowwise_adagrad", 0.01, 1e-8, 0.1, dynamic=True),
+            ci.TableSpec(2048, 64, "bf16", "sum", "adagrad", 0.02, 1e-8, 0.0, master=True, dynamic=True),
+            ci.TableSpec(1024, 8, "f16", "sum", "sgd", 0.01, dynamic=True)]
+    lens = np.random.default_rng(seed).integers(0, 9, size=len(tabs) * B)
+
+    def keys(rng, t, s, L):
+        k = rng.integers(0, s.key_space, L)
+        k[rng.random(L) < 0.25] = 3
+        return ci.dynamic_key(t, k) if s.dynamic else k
+
+    return _custom(tabs, B, lens, keys, seed=seed)
+
+
+def _dynamic_reference(w, b, g, seed):
+    lo, hi = w.w_lo, w.w_hi
+    return oracle.step_dynamic(
+        w.tables, w.batch, b.offsets, b.keys, b.table_ids, g, init_rows_fn(w, seed),
+        lambda t, k: ci.init_values_dynamic(seed, t, k, w.tables[t].dim, lo, hi, w.tables[t].dtype),
+        None, lambda t, k: ci.init_values_dynamic(seed, t, k, w.tables[t].dim, lo, hi, "f32"))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_dynamic_tables_parity(variant):
+    import torch
+    w, b, g = _dynamic_inputs()
+    seed = 0
+    gs = run_gpu_step(w, b, g, variant, seed, keep_layer=True)
+    layer = gs.layer
+    try:
+        assert gs.status_fwd == 0 and gs.status_bwd == 0
+        ref, key_of = _dynamic_reference(w, b, g, seed)
+        assert max_rel_err(gs.out, ref.out, ref.out_scale) <= 1e-5
+        # one unique row per distinct key of each table, with the same counts
+        assert gs.unique.size == ref.unique.size
+        assert np.array_equal(np.sort(gs.counts), np.sort(ref.counts))
+        for t, spec in enumerate(w.tables):
+            sel = np.nonzero(ref.rows.table == t)[0]
+            idx = ref.rows.row_start[sel][:, None] + np.arange(spec.dim)[None, :]
+            rows = ref.rows.row[sel]
+            if spec.dynamic:
+                rows = layer.find_keys(t, torch.from_numpy(key_of[t][rows]).cuda()).cpu().numpy()
+                assert np.all(rows >= 0) and np.unique(rows).size == rows.size
+            W, A = gather_rows(layer, w, t, rows)
+            assert max_rel_err(W, ref.W[idx], ref.W_scale[idx]) <= TOL[spec.dtype], t
+            if spec.opt != "sgd":
+                ra, rs = ref_state(spec, ref.A, ref.A_scale, idx)
+                assert max_rel_err(A, ra, rs) <= 1e-5, t
+            if spec.master:
+                M = layer.gather_master_rows(t, torch.from_numpy(rows).cuda()).cpu().numpy()
+                assert max_rel_err(M, ref.M[idx], ref.W_scale[idx]) <= 1e-5, t
+    finally:
+        layer.close()
+
+
+def test_dynamic_first_lookup_initializes_rows_once():
+    import torch
+    from dlrm_sparse_embedding_gb300 import EMB_OK, EmbeddingLayer
+    w, b, _ = _dynamic_inputs(B=400, seed=22)
+    layer = EmbeddingLayer(w.tables, w.batch, b.nnz)
+    try:
+        layer.init_uniform(7, -0.05, 0.05)
+        k, o, tid = (torch.from_numpy(x).cuda() for x in (b.keys, b.offsets, b.table_ids))
+        layer.forward(k, o, tid, w.batch)
+        assert layer.sync_status() == EMB_OK
+        for t, spec in enumerate(w.tables):
+            if not spec.dynamic:
+                continue
+            seg = b.keys[b.offsets[t * w.batch]:b.offsets[(t + 1) * w.batch]]
+            uk = np.unique(seg)
+            rows = layer.find_keys(t, torch.from_numpy(uk).cuda()).cpu().numpy()
+            assert np.all(rows >= 0) and np.unique(rows).size == uk.size
+            W, A = layer.gather_rows(t, torch.from_numpy(rows).cuda(), with_state=spec.opt != "sgd")
+            want = ci.init_values_dynamic(7, t, uk, spec.dim, -0.05, 0.05, spec.dtype)
+            got = W.view(torch.int16).cpu().numpy().view(np.uint16) if spec.dtype == "bf16" else W.cpu().numpy()
+            assert np.array_equal(got.view(np.uint16) if spec.dtype != "f32" else got,
+                                  want.view(np.uint16) if spec.dtype != "f32" else want)
+            if A is not None:
+                assert np.all(A.cpu().numpy() == np.float32(spec.init_acc))
+            if spec.master:
+                M = layer.gather_master_rows(t, torch.from_numpy(rows).cuda()).cpu().numpy()
+                assert np.array_equal(M, ci.init_values_dynamic(7, t, uk, spec.dim, -0.05, 0.05, "f32"))
+            # keys already held keep their rows; keys never seen have none
+            layer.forward(k, o, tid, w.batch)
+            again = layer.find_keys(t, torch.from_numpy(uk).cuda()).cpu().numpy()
+            assert np.array_equal(again, rows)
+            absent = ci.dynamic_key(t, np.arange(spec.key_space, spec.key_space + 50))
+            assert np.all(layer.find_keys(t, torch.from_numpy(absent).cuda()).cpu().numpy() == -1)
+    finally:
+        layer.close()
+
+
+def test_dynamic_table_full_and_reserved_key_are_reported():
+    import torch
+    from dlrm_sparse_embedding_gb300 import EMB_ERR_CAPACITY, EMB_ERR_KEY_RANGE, EmbeddingLayer
+    tabs = [ci.TableSpec(64, 8, "f32", "sum", "sgd", 0.01, dynamic=True)]
+    B = 100
+    keys = ci.dynamic_key(0, np.arange(B))              # 100 distinct keys, 64 rows
+    offsets = np.arange(B + 1, dtype=np.int64)
+    tid = np.zeros(B, np.int32)
+    layer = EmbeddingLayer(tabs, B, B)
+    try:
+        layer.init_uniform(0, -0.05, 0.05)
+        kt = torch.from_numpy(keys).cuda()
+        out = layer.forward(kt, torch.from_numpy(offsets).cuda(), torch.from_numpy(tid).cuda(), B)
+        assert layer.sync_status() == EMB_ERR_CAPACITY
+        rows = layer.find_keys(0, kt).cpu().numpy()
+        held = rows >= 0
+        assert held.sum() == 64 and np.unique(rows[held]).size == 64
+        assert np.all(out.cpu().numpy()[~held] == 0)          # lookups that found no row are skipped
+        keys2 = keys.copy()
+        keys2[5] = np.iinfo(np.int64).min                   # the reserved key
+        layer.init_uniform(0, -0.05, 0.05)                   # empties the map
+        layer.forward(torch.from_numpy(keys2[:60]).cuda(), torch.from_numpy(offsets[:61]).cuda(),
+                      torch.from_numpy(tid[:60]).cuda(), 60)
+        assert layer.sync_status() == EMB_ERR_KEY_RANGE
+    finally:
+        layer.close()

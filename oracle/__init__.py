@@ -371,3 +371,22 @@ def step_dynamic(tables, B: int, offsets, keys, table_ids, grad_out,
     if init_master is not None or init_dynamic_master is not None:
         master_fn = lambda t, r: (init_dynamic_master(t, key_of[t][r]) if t in key_of else init_master(t, r))
     return step(tables2, B, offsets, keys2, table_ids, grad_out, rows_fn, master_fn), key_of
+
+
+def forward_with_cache(tables, B: int, offsets, keys, table_ids,
+                       init_rows: Callable[[int, np.ndarray], np.ndarray], cached: dict):
+    """Inference forward with fp16 caches: the pooled output (a1) over the
+    tables with every row in cached[t] (row ids of table t) replaced by its
+    nearest-even fp16 rounding (NumPy's conversion), as a cache of those rows
+    would serve it.  Returns (out, out_scale)."""
+    gids, _ = global_ids(tables, B, offsets, keys, table_ids)
+    uniq, inv, _, _ = unique(gids, skip_negative=True)
+
+    def values(t, r):
+        v = stored_to_f64(init_rows(t, r), tables[t].dtype)
+        hit = np.isin(np.asarray(r), np.asarray(cached.get(t, []), dtype=np.int64))
+        v[hit] = v[hit].astype(np.float16).astype(np.float64)
+        return v.astype(np.float32)
+
+    rows = make_row_store(tables, uniq, values, fp32_values=True)
+    return forward(tables, B, offsets, inv, rows, want_scale=True)

@@ -521,6 +521,31 @@ def test_dynamic_table_is_the_static_table_over_its_keys():
         assert np.array_equal(res.A[a:a + dim], ref.A[b:b + dim])
 
 
+def test_forward_with_cache_reduces_to_the_plain_forward():
+    # no cached rows: the training forward's output exactly; every row cached
+    # but the table already fp16: unchanged again; an fp32 table's cached row
+    # contributes its fp16 rounding
+    B, dim = 64, 8
+    offsets, keys, tid = _random_csr(2, B, [40, 40], 4, 71)
+    rng = np.random.default_rng(72)
+    W32 = rng.uniform(-0.05, 0.05, (40, dim)).astype(np.float32)
+    W16 = rng.uniform(-0.05, 0.05, (40, dim)).astype(np.float16)
+    tables = [_spec(40, dim), _spec(40, dim, dtype="f16")]
+    init = lambda t, r: (W32 if t == 0 else W16)[r]
+    grad = np.zeros((B, 2 * dim), np.float32)
+    plain = oracle.step(tables, B, offsets, keys, tid, grad, init).out
+    out0, _ = oracle.forward_with_cache(tables, B, offsets, keys, tid, init, {})
+    assert np.array_equal(out0, plain)
+    out1, _ = oracle.forward_with_cache(tables, B, offsets, keys, tid, init, {1: np.arange(40)})
+    assert np.array_equal(out1, plain)
+    # one-hot bags of table 0 holding row 3 now pool its fp16 value
+    one = np.arange(B + 1, dtype=np.int64)
+    k1 = np.full(B, 3, np.int64)
+    t1 = [_spec(40, dim)]
+    out2, _ = oracle.forward_with_cache(t1, B, one, k1, np.zeros(B, np.int32), lambda t, r: W32[r], {0: [3, 7]})
+    assert np.array_equal(out2, np.broadcast_to(W32[3].astype(np.float16).astype(np.float32), (B, dim)))
+
+
 def _torch_reference_step(tables, B, offsets, keys, grad, W, opt_name):
     """Independent reference: torch embedding_bag (float64, sparse grads) + torch.optim."""
     outs, params = [], []

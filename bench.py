@@ -252,6 +252,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--early-dedup", action="store_true",
                     help="run the dedup inside the forward on the layer's second stream (overlap)")
+    ap.add_argument("--infer", action="store_true",
+                    help="also time the inference-only forward with fp16 caches of each table's hottest rows")
+    ap.add_argument("--cache-frac", type=float, default=0.01,
+                    help="share of each static table's rows (the hottest ranks) held in its inference cache")
     ap.add_argument("--batch", type=int, default=0, help="override the batch size (small profiling cases)")
     ap.add_argument("--rows-cap", type=int, default=0, help="cap every table's rows (small profiling cases)")
     args = ap.parse_args()
@@ -337,6 +341,36 @@ def main():
     layer.set_timing(False)
     status = layer.sync_status()
     ms = max_over_ranks(ms, dev)
+
+    # ---- inference-only forward with fp16 hot-row caches (optional) ----
+    infer = None
+    if args.infer:
+        cached_rows = 0
+        for t, s_ in enumerate(w.tables):
+            if getattr(s_, "dynamic", False):
+                continue
+            n_c = max(1, int(s_.rows * args.cache_frac))        # Zipf rank 0 is the hottest row
+            layer.cache_build(t, torch.arange(n_c, dtype=torch.int64, device=dev))
+            cached_rows += n_c
+        for i in range(args.warmup):
+            layer.forward_infer(dkeys[i % args.batches], doffs[i % args.batches], dtids[i % args.batches], w.batch, out)
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for i in range(args.steps):
+            k_ = i % args.batches
+            layer.forward_infer(dkeys[k_], doffs[k_], dtids[k_], w.batch, out)
+        f1.record()
+        torch.cuda.synchronize()
+        ims = max_over_ranks(f0.elapsed_time(f1) / args.steps, dev)
+        # compulsory bytes: keys, offsets, table ids, each touched row once, the output, a code per lookup
+        ibytes = bytes_["forward"] - 8 * batches[0].nnz + 16 * batches[0].nnz
+        infer = {"metric": "inference lookups/s (pooled forward, fp16 caches of the hottest rows)",
+                 "value": whole_job_rate(batches[0].nnz, ws, ims), "unit": "lookups/s", "ms_per_step": ims,
+                 "cache": "hottest %.2f%% of each static table's rows as fp16 (%d rows)" % (100 * args.cache_frac,
+                                                                                          cached_rows),
+                 "hbm": {"algorithmic_bytes": ibytes, "achieved_gbs": ibytes / (ims / 1e3) / 1e9},
+                 "status": layer.sync_status()}
 
     # ---- end to end: host buffers, copies inside the timed region ----
     # Every step copies its inputs (keys, offsets, table ids, grad_out) from
@@ -477,6 +511,7 @@ def main():
                      "algorithmic_bytes": bytes_[dom], "peak_kind": peak_kind},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        **({"infer": infer} if infer is not None else {}),
         "gpu_launches": launches,
         "clocks": clk,
         "status": status,

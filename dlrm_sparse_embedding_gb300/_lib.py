@@ -31,7 +31,8 @@ EXPORTS = (
     "emb_set_keep_dedup", "emb_dedup_result", "emb_unique_workspace", "emb_unique",
     "emb_get_rows", "emb_set_rows", "emb_gather_rows", "emb_sync_status", "emb_launch_count",
     "emb_set_timing", "emb_phase_times", "emb_unique_noalloc", "emb_set_early_dedup",
-    "emb_get_master_rows", "emb_set_master_rows", "emb_gather_master_rows", "emb_find_keys", "emb_status_string",
+    "emb_get_master_rows", "emb_set_master_rows", "emb_gather_master_rows", "emb_find_keys",
+    "emb_cache_build", "emb_forward_infer", "emb_status_string",
 )
 UNIQUE_NOALLOC_MAX_KEYS = 262144
 PHASES = ("forward", "dedup", "reduce_update")
@@ -81,6 +82,8 @@ def _load() -> ctypes.CDLL:
     L.emb_set_master_rows.argtypes = [vp, i32, i64, i64, vp, vp]
     L.emb_gather_master_rows.argtypes = [vp, i32, vp, i64, vp, vp]
     L.emb_find_keys.argtypes = [vp, i32, vp, i64, vp, vp]
+    L.emb_cache_build.argtypes = [vp, i32, vp, i64, vp]
+    L.emb_forward_infer.argtypes = [vp, vp, vp, vp, i64, i32, vp, vp]
     L.emb_sync_status.argtypes = [vp, vp]
     L.emb_launch_count.argtypes = [vp, ctypes.POINTER(i64), i32]
     L.emb_set_timing.argtypes = [vp, i32]

@@ -41,6 +41,10 @@ struct TableDev {
     int32_t doff;        // column offset in the concatenated output
     int32_t dynamic;     // 1: keys are int64 ids mapped to rows by map_keys
     unsigned long long* map_keys;   // dynamic tables: [rows] key held by each row (kMapEmpty = free)
+    const __half* cache_w;          // inference cache: [cache rows][dim] fp16 copies of chosen rows, or null
+    const unsigned long long* cache_map;   // open addressing: (row << 32) | cache slot, kCacheEmpty = free
+    uint32_t cache_mask;            // cache_map has cache_mask + 1 entries (a power of two)
+    int32_t pad2_;
 };
 
 // ---------------------------------------------------------------------------
@@ -254,6 +258,7 @@ struct FwdArgs {
     bool write_ids;             // the pooling kernel also writes gid_out / bag_out
     bool rows16;                // every table stores 16-bit rows (selects the pooling kernel's occupancy)
     const int64_t* resolved;    // dynamic tables: row of each lookup (-1: none), read instead of keys
+    bool infer;                 // the inference forward (reads caches, writes nothing for a backward)
     int* err;
 };
 
@@ -286,6 +291,31 @@ int launch_dyn_find(const TableDev* tables, int t, const int64_t* keys, int64_t 
                     cudaStream_t st);
 // Marks every row of a map free.
 int launch_dyn_clear(unsigned long long* map_keys, int64_t rows, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// inference forward with fp16 caches of chosen rows (infer.cu)
+// ---------------------------------------------------------------------------
+constexpr unsigned long long kCacheEmpty = ~0ull;
+
+// Fills table t's cache from n row ids (device): slot i holds row rows[i] in
+// fp16 (rows held twice keep their first slot); cache_map must be all
+// kCacheEmpty.  Returns kernels launched or -1.
+int launch_cache_fill(const TableDev& tb, int t, const int64_t* rows, int64_t n, __half* cache_w,
+                      unsigned long long* cache_map, uint32_t cache_mask, int* err, cudaStream_t st);
+
+struct InferArgs {
+    const int64_t* keys;
+    const int64_t* offsets;
+    int32_t batch;
+    const TableDev* tables;
+    const int32_t* dyn_tables;  // [num_dyn] indices of the dynamic tables
+    int32_t num_dyn;
+    int64_t* resolved;          // [nnz] row of each lookup of a dynamic table (-1: never seen)
+};
+
+// Rows of the dynamic tables' keys for the inference forward, found without
+// inserting.  Returns kernels launched or -1.
+int launch_infer_resolve(const InferArgs& a, int64_t nnz, cudaStream_t st);
 int launch_forward_ids(const FwdArgs& a, cudaStream_t st);   // gid_out / bag_out only
 
 // dedup helpers (dedup.cu); each returns kernels launched or -1

@@ -96,10 +96,43 @@ __device__ __forceinline__ void close_bags(BagStream& st, int64_t pos, int nbg, 
     }
 }
 
+// The row of a lookup code in the inference forward: a table row, or (high
+// bit set, tables with a cache) a row of the table's fp16 cache.
+__device__ __forceinline__ float4 load_cached_row4(const TableDev& tb, uint32_t slot, int li)
+{
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(tb.cache_w + (int64_t)slot * tb.dim + 4 * li));
+    const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+
+constexpr uint32_t kCacheBit = 0x80000000u;
+
+// Cache slot of `row` in its table's inference cache, or -1 (bounded probe of
+// the open-addressing map of (row << 32 | slot) entries).
+__device__ __forceinline__ int64_t cache_slot_of(const TableDev& tb, int64_t row)
+{
+    uint64_t z = (uint64_t)row + 0x632BE59BD9B4E019ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    uint32_t s = (uint32_t)(z ^ (z >> 31)) & tb.cache_mask;
+    for (uint32_t probe = 0; probe <= tb.cache_mask; ++probe) {
+        const unsigned long long e = __ldg(tb.cache_map + s);
+        if (e == kCacheEmpty) return -1;
+        if ((e >> 32) == (unsigned long long)row) return (int64_t)(e & 0xFFFFFFFFull);
+        s = (s + 1) & tb.cache_mask;
+    }
+    return -1;
+}
+
 // kMinBlocks: resident blocks per SM the register budget is sized for.  With
 // 16-bit rows a lane holds half the row data in flight, and 4 blocks (64
 // registers) measure faster; fp32 rows take 3 (80 registers).
-template <int kMinBlocks>
+// kInfer: the inference forward.  A row held in its table's cache is read
+// from the fp16 cache (the lane that loads the key probes the cache map), a
+// dynamic table's id it never saw is skipped silently, and nothing is written
+// for a backward (no ids, no bag scales).
+template <int kMinBlocks, bool kInfer>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
 {
     const int lane = threadIdx.x & 31;
@@ -136,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
     if (li < nbg) {
         my_len = (int)(my_end - my_start);
         if (!my_tid_ok) atomicOr(a.err, ERRBIT_TABLE_ID);
-        if (mean) a.bag_scale[j0 + li] = my_len > 0 ? __frcp_rn((float)my_len) : 0.f;
+        if (mean && !kInfer) a.bag_scale[j0 + li] = my_len > 0 ? __frcp_rn((float)my_len) : 0.f;
     }
     const int64_t K1 = __shfl_sync(gmask, my_end, nbg - 1, Lr);
     float* const out_col = a.out + tb.doff + 4 * li;
@@ -146,15 +179,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
         // its pooled value is the row itself, so rows go straight to the output
         const int64_t i = K0 + li;
         const bool in = li < nbg;
-        const int64_t key = in ? __ldg(kp + i) : 0;
+        int64_t key = in ? __ldg(kp + i) : 0;
         const bool valid = in && my_tid_ok && key >= 0 && key < tb.rows;
-        if (valid) prefetch_row_l2(tb, key);
+        if (kInfer && valid && tb.cache_map) {
+            const int64_t cs = cache_slot_of(tb, key);
+            if (cs >= 0) key = -cs - 2;   // a cached row: its cache slot, coded below zero
+        }
+        if (valid && key >= 0) prefetch_row_l2(tb, key);
         if (in) {
-            if (a.write_ids) {
+            if (!kInfer && a.write_ids) {
                 a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
                 a.bag_out[i] = (uint32_t)(j0 + li);
             }
-            if (!valid && my_tid_ok) atomicOr(a.err, ERRBIT_KEY_RANGE);
+            if (!valid && my_tid_ok && !(kInfer && tb.dynamic)) atomicOr(a.err, ERRBIT_KEY_RANGE);
         }
         for (int q = 0; q < nbg; q += kPrefetch) {
             float4 v[kPrefetch];
@@ -164,7 +201,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
                 const int64_t kq = __shfl_sync(gmask, key, qq & (Lr - 1), Lr);
                 const bool vq = __shfl_sync(gmask, valid, qq & (Lr - 1), Lr) && qq < nbg;
                 v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (vq && colok) v[u] = load_row4(tb.w, tb.dtype, kq * tb.dim + 4 * li);
+                if (vq && colok)
+                    v[u] = (kInfer && kq < 0) ? load_cached_row4(tb, (uint32_t)(-kq - 2), li)
+                                              : load_row4(tb.w, tb.dtype, kq * tb.dim + 4 * li);
             }
 #pragma unroll
             for (int u = 0; u < kPrefetch; ++u)
@@ -195,16 +234,22 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
         const int64_t kend = __shfl_sync(gmask, my_end, k, Lr);
         const bool valid = in && tok && key >= 0 && key < tb.rows;
         if (in) {
-            if (a.write_ids) {
+            if (!kInfer && a.write_ids) {
                 a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
                 a.bag_out[i] = (uint32_t)(j0 + k);
             }
-            if (!valid && tok) atomicOr(a.err, ERRBIT_KEY_RANGE);
+            if (!valid && tok && !(kInfer && tb.dynamic)) atomicOr(a.err, ERRBIT_KEY_RANGE);
         }
         // bit u: a bag ends right after position base + u
         const uint32_t endbits = (__ballot_sync(gmask, in && kend == i + 1) >> (g * Lr)) & lowmask;
-        // rows < 2^32 per table, so a key travels as 32 bits; kNoRow = skipped
-        const uint32_t kk = valid ? (uint32_t)key : kNoRow;
+        // rows < 2^32 per table, so a key travels as 32 bits; kNoRow = skipped.
+        // A cache slot (tables with a cache have fewer than 2^31 rows) travels
+        // with kCacheBit set.
+        uint32_t kk = valid ? (uint32_t)key : kNoRow;
+        if (kInfer && valid && tb.cache_map) {
+            const int64_t cs = cache_slot_of(tb, key);
+            if (cs >= 0) kk = kCacheBit | (uint32_t)cs;
+        }
         const int cnt = (int)((K1 - base) < Lr ? (K1 - base) : Lr);
         for (int q = 0; q < cnt; q += kPrefetch) {
             float4 v[kPrefetch];
@@ -212,7 +257,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
             for (int u = 0; u < kPrefetch; ++u) {
                 const uint32_t kq = __shfl_sync(gmask, kk, (q + u) & (Lr - 1), Lr);
                 v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (kq != kNoRow && q + u < cnt && colok) v[u] = load_row4(tb.w, tb.dtype, (int64_t)kq * tb.dim + 4 * li);
+                if (kq != kNoRow && q + u < cnt && colok)
+                    v[u] = (kInfer && tb.cache_w && (kq & kCacheBit))
+                               ? load_cached_row4(tb, kq & ~kCacheBit, li)
+                               : load_row4(tb.w, tb.dtype, (int64_t)kq * tb.dim + 4 * li);
             }
             // rows are added in pairs, then compensated into the bag's sum; a
             // bag ending inside a pair takes the first row alone
@@ -294,10 +342,17 @@ int launch_forward(const FwdArgs& a, cudaStream_t st)
     const int64_t warps = a.warps_per_table * a.num_tables;
     if (warps <= 0) return 0;
     const unsigned blocks = (unsigned)((warps * 32 + kThreads - 1) / kThreads);
-    if (a.rows16)
-        fwd_pool<4><<<blocks, kThreads, 0, st>>>(a);
-    else
-        fwd_pool<3><<<blocks, kThreads, 0, st>>>(a);
+    if (a.infer) {
+        if (a.rows16)
+            fwd_pool<4, true><<<blocks, kThreads, 0, st>>>(a);
+        else
+            fwd_pool<3, true><<<blocks, kThreads, 0, st>>>(a);
+    } else {
+        if (a.rows16)
+            fwd_pool<4, false><<<blocks, kThreads, 0, st>>>(a);
+        else
+            fwd_pool<3, false><<<blocks, kThreads, 0, st>>>(a);
+    }
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

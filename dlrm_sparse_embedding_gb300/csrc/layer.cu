@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "emb_internal.cuh"
@@ -60,6 +61,8 @@ struct emb_layer {
     int64_t* resolved = nullptr;      // [max_nnz] row of each lookup of a dynamic table
     uint64_t dyn_seed = 0;            // initial values of rows inserted later (last emb_init_uniform)
     float dyn_lo = 0.f, dyn_hi = 0.f;
+    // inference caches (infer.cu): per table its fp16 rows and map, freed on rebuild
+    std::vector<std::pair<void*, void*>> cache_bufs;
 
     std::vector<void*> allocs;
     size_t alloc_bytes = 0;
@@ -345,6 +348,7 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
     uint64_t rb = 0;
     int32_t doff = 0;
     L->tabs.resize(num_tables);
+    L->cache_bufs.assign(num_tables, std::make_pair(nullptr, nullptr));
     for (int t = 0; t < num_tables && ok; ++t) {
         const emb_table_spec& s = specs[t];
         TableDev& d = L->tabs[t];
@@ -359,6 +363,10 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
         d.doff = doff;
         d.dynamic = s.dynamic;
         d.map_keys = nullptr;
+        d.cache_w = nullptr;
+        d.cache_map = nullptr;
+        d.cache_mask = 0;
+        d.pad2_ = 0;
         d.w = nullptr;
         d.state = nullptr;
         d.master = nullptr;
@@ -444,6 +452,10 @@ int emb_destroy(emb_layer* L)
     if (L->ev_in) cudaEventDestroy(L->ev_in);
     if (L->ev_ready) cudaEventDestroy(L->ev_ready);
     if (L->side) cudaStreamDestroy(L->side);
+    for (auto& cb : L->cache_bufs) {
+        if (cb.first) cudaFree(cb.first);
+        if (cb.second) cudaFree(cb.second);
+    }
     free_all(L);
     delete L;
     return EMB_OK;
@@ -554,6 +566,7 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
     a.write_ids = true;
     a.rows16 = true;
     a.resolved = L->resolved;
+    a.infer = false;
     for (const TableDev& d : L->tabs) a.rows16 = a.rows16 && d.dtype != EMB_F32;
     a.err = L->err;
     if (L->timing) harvest_timing(L);
@@ -791,6 +804,88 @@ int emb_set_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, const void* w
                              cudaMemcpyHostToDevice, st) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
     return ok ? EMB_OK : EMB_ERR_CUDA;
+}
+
+int emb_cache_build(emb_layer* L, int32_t t, const int64_t* rows, int64_t n, void* stream)
+{
+    if (!L || t < 0 || t >= L->T || n < 0 || n >= (int64_t(1) << 30) || (n > 0 && !rows) ||
+        (n > 0 && L->tabs[t].rows >= (int64_t(1) << 31)))
+        return EMB_ERR_INVALID_ARG;
+    cudaStream_t st = S(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return EMB_ERR_CUDA;
+    TableDev& d = L->tabs[t];
+    auto& cb = L->cache_bufs[t];
+    if (cb.first) cudaFree(cb.first);
+    if (cb.second) cudaFree(cb.second);
+    cb = std::make_pair(nullptr, nullptr);
+    d.cache_w = nullptr;
+    d.cache_map = nullptr;
+    d.cache_mask = 0;
+    int rc = EMB_OK;
+    if (n > 0) {
+        uint64_t cap = 64;
+        while (cap < 2 * (uint64_t)n) cap <<= 1;
+        void *w = nullptr, *m = nullptr;
+        if (cudaMalloc(&w, sizeof(__half) * (size_t)n * d.dim) != cudaSuccess ||
+            cudaMalloc(&m, sizeof(unsigned long long) * cap) != cudaSuccess) {
+            cudaGetLastError();
+            if (w) cudaFree(w);
+            rc = EMB_ERR_OOM;
+        } else {
+            cb = std::make_pair(w, m);
+            d.cache_mask = (uint32_t)(cap - 1);
+            if (cudaMemsetAsync(m, 0xFF, sizeof(unsigned long long) * cap, st) != cudaSuccess) rc = EMB_ERR_CUDA;
+            if (rc == EMB_OK)
+                rc = track(L, launch_cache_fill(d, t, rows, n, static_cast<__half*>(w),
+                                                static_cast<unsigned long long*>(m), d.cache_mask, L->err, st));
+            d.cache_w = static_cast<const __half*>(w);
+            d.cache_map = static_cast<const unsigned long long*>(m);
+        }
+    }
+    if (cudaMemcpyAsync(L->d_tables + t, &d, sizeof(TableDev), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        rc = EMB_ERR_CUDA;
+    return rc;
+}
+
+int emb_forward_infer(emb_layer* L, const int64_t* keys, const int64_t* offsets, const int32_t* table_ids,
+                      int64_t nnz, int32_t batch, float* out, void* stream)
+{
+    if (!L || !offsets || !table_ids || !out || batch < 1 || batch > L->max_batch || nnz < 0 || nnz > L->max_nnz ||
+        (nnz > 0 && !keys) || !aligned16(out))
+        return EMB_ERR_INVALID_ARG;
+    cudaStream_t st = S(stream);
+    InferArgs ia;
+    ia.keys = keys;
+    ia.offsets = offsets;
+    ia.batch = batch;
+    ia.tables = L->d_tables;
+    ia.dyn_tables = L->d_dyn_tables;
+    ia.num_dyn = L->num_dyn;
+    ia.resolved = L->resolved;
+    int rc = track(L, launch_infer_resolve(ia, nnz, st));
+    if (rc != EMB_OK) return rc;
+    FwdArgs a;
+    a.keys = keys;
+    a.offsets = offsets;
+    a.table_ids = table_ids;
+    a.batch = batch;
+    a.num_tables = L->T;
+    a.out = out;
+    a.ld = L->total_dim;
+    a.tables = L->d_tables;
+    a.gid_out = nullptr;
+    a.bag_out = nullptr;
+    a.bag_scale = nullptr;
+    a.sentinel = (uint32_t)L->total_rows;
+    a.warps_per_table = (batch + 31) / 32;
+    a.write_ids = false;
+    a.rows16 = true;
+    for (const TableDev& d : L->tabs) a.rows16 = a.rows16 && d.dtype != EMB_F32;
+    a.resolved = L->resolved;
+    a.infer = true;
+    a.err = L->err;
+    return track(L, launch_forward(a, st));
 }
 
 int emb_find_keys(emb_layer* L, int32_t t, const int64_t* keys, int64_t n, int64_t* rows_out, void* stream)

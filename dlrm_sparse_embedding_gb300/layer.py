@@ -171,6 +171,24 @@ class EmbeddingLayer:
                                None if s is None else s.ctypes.data_as(ctypes.c_void_p), _stream(stream)),
               "emb_set_rows")
 
+    # -- inference ------------------------------------------------------------------
+    def cache_build(self, t: int, rows: torch.Tensor, stream=None) -> None:
+        """fp16 inference cache of the given rows (int64, device) of table t (empty: none)."""
+        n = int(rows.numel())
+        check(lib.emb_cache_build(self._h, t, _ptr(rows) if n else None, n, _stream(stream)), "emb_cache_build")
+
+    def forward_infer(self, keys: torch.Tensor, offsets: torch.Tensor, table_ids: torch.Tensor, batch: int,
+                      out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """Pooled output reading cached rows from the fp16 caches; keeps nothing for a backward."""
+        if out is None:
+            out = torch.empty((batch, self.total_dim), dtype=torch.float32, device=offsets.device)
+        assert keys.dtype == torch.int64 and offsets.dtype == torch.int64 and table_ids.dtype == torch.int32
+        assert out.dtype == torch.float32 and out.shape == (batch, self.total_dim)
+        nnz = int(keys.numel())
+        check(lib.emb_forward_infer(self._h, _ptr(keys) if nnz else None, _ptr(offsets), _ptr(table_ids), nnz,
+                                    int(batch), _ptr(out), _stream(stream)), "emb_forward_infer")
+        return out
+
     # -- dynamic tables -----------------------------------------------------------
     def find_keys(self, t: int, keys: torch.Tensor, stream=None) -> torch.Tensor:
         """Rows (int64, -1 when absent) of int64 keys of dynamic table t; inserts nothing."""

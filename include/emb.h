@@ -244,6 +244,29 @@ int emb_get_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n, void* wei
 int emb_set_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n,
                  const void* weights_host, const float* state_host, void* stream);
 
+/* Inference cache of table t (the HPS / embedding-cache idea of the Merlin
+ * overview article, section on HugeCTR inference): fp16 copies of n chosen
+ * rows (device int64 row ids; a dynamic table's rows from emb_find_keys),
+ * looked up through a hash map from row to cache slot.  Replaces any earlier
+ * cache of the table; n = 0 removes it.  The copies are a snapshot of the
+ * rows at this call (16-bit tables are converted from their stored values
+ * to fp16): training steps do not refresh them.  Tables of 2^31 rows or more
+ * take no cache (EMB_ERR_INVALID_ARG).  Allocates device memory for the cache
+ * and synchronises `stream`; EMB_ERR_OOM when it cannot allocate.
+ * An id outside [0, rows) is skipped and flagged like a bad key. */
+int emb_cache_build(emb_layer* layer, int32_t t, const int64_t* rows, int64_t n, void* stream);
+
+/* Inference-only forward: the pooled, concatenated output of emb_forward
+ * (same arguments, layout and error reporting), reading every row held in
+ * its table's cache from the fp16 cache and every other row from the table.
+ * Dynamic tables look keys up without inserting; an id the table does not
+ * hold contributes nothing and is not an error.  Nothing is kept for a
+ * backward: a following emb_backward_update still refers to the last
+ * emb_forward.  Allocates nothing. */
+int emb_forward_infer(emb_layer* layer, const int64_t* keys, const int64_t* offsets,
+                      const int32_t* table_ids, int64_t nnz, int32_t batch, float* out,
+                      void* stream);
+
 /* Rows of n keys (device int64) of dynamic table t, into rows_out (device
  * int64; -1 for a key the table does not hold).  Inserts nothing.
  * Asynchronous; EMB_ERR_INVALID_ARG for a table that is not dynamic. */

@@ -553,3 +553,82 @@ def test_dynamic_table_full_and_reserved_key_are_reported():
         assert layer.sync_status() == EMB_ERR_KEY_RANGE
     finally:
         layer.close()
+
+
+# ---------------------------------------------------------------------------
+# inference forward with fp16 caches of hot rows
+# ---------------------------------------------------------------------------
+
+def test_forward_infer_with_caches():
+    import torch
+    from dlrm_sparse_embedding_gb300 import EMB_ERR_KEY_RANGE, EMB_OK, EmbeddingLayer
+    tabs = [ci.TableSpec(3000, 128, "f32", "sum", "adagrad"), ci.TableSpec(900, 16, "bf16", "mean", "sgd"),
+            ci.TableSpec(500, 64, "f16", "sum", "sgd"), ci.TableSpec(60, 20, "f32", "mean", "sgd")]
+    B = 700
+    lens = np.random.default_rng(31).integers(0, 7, size=len(tabs) * B)
+
+    def keys(rng, t, s, L):
+        k = rng.integers(0, s.rows, L)
+        k[rng.random(L) < 0.4] = 2                          # a hot row, cached in two tables
+        return k
+
+    w, b, _ = _custom(tabs, B, lens, keys, seed=32)
+    cached = {0: np.arange(30), 1: np.array([2, 2, 5, 899, 800, 3]), 3: np.arange(60)}
+    seed = 0
+    layer = EmbeddingLayer(w.tables, B, b.nnz)
+    try:
+        layer.init_uniform(seed, w.w_lo, w.w_hi)
+        k, o, tid = (torch.from_numpy(x).cuda() for x in (b.keys, b.offsets, b.table_ids))
+        for t, rows in cached.items():
+            layer.cache_build(t, torch.from_numpy(rows.astype(np.int64)).cuda())
+        got = layer.forward_infer(k, o, tid, B).cpu().numpy()
+        assert layer.sync_status() == EMB_OK
+        want, scale = oracle.forward_with_cache(w.tables, B, b.offsets, b.keys, b.table_ids, init_rows_fn(w, seed),
+                                                cached)
+        assert max_rel_err(got, want, scale) <= 1e-5
+        # the training forward still reads the tables
+        plain = layer.forward(k, o, tid, B).cpu().numpy()
+        want0, scale0 = oracle.forward_with_cache(w.tables, B, b.offsets, b.keys, b.table_ids,
+                                                  init_rows_fn(w, seed), {})
+        assert max_rel_err(plain, want0, scale0) <= 1e-5
+        # removing the caches: inference reads the tables too
+        for t in cached:
+            layer.cache_build(t, torch.zeros(0, dtype=torch.int64).cuda())
+        assert max_rel_err(layer.forward_infer(k, o, tid, B).cpu().numpy(), want0, scale0) <= 1e-5
+        # a row id outside the table is reported
+        layer.cache_build(2, torch.tensor([1, 500], dtype=torch.int64).cuda())
+        assert layer.sync_status() == EMB_ERR_KEY_RANGE
+    finally:
+        layer.close()
+
+
+def test_forward_infer_on_dynamic_tables_skips_unseen_ids():
+    import torch
+    from dlrm_sparse_embedding_gb300 import EMB_OK, EmbeddingLayer
+    w, b, g = _dynamic_inputs(B=300, seed=33)
+    seed = 0
+    layer = EmbeddingLayer(w.tables, w.batch, b.nnz)
+    try:
+        layer.init_uniform(seed, w.w_lo, w.w_hi)
+        k, o, tid = (torch.from_numpy(x).cuda() for x in (b.keys, b.offsets, b.table_ids))
+        layer.forward(k, o, tid, w.batch)                   # inserts every key
+        # a second batch whose dynamic keys are half new
+        keys2 = b.keys.copy()
+        for t, spec in enumerate(w.tables):
+            if spec.dynamic:
+                lo_, hi_ = b.offsets[t * w.batch], b.offsets[(t + 1) * w.batch]
+                flip = np.random.default_rng(t).random(hi_ - lo_) < 0.5
+                keys2[lo_:hi_][flip] = ci.dynamic_key(t, np.arange(spec.key_space, spec.key_space + flip.sum()))
+        got = layer.forward_infer(torch.from_numpy(keys2).cuda(), o, tid, w.batch).cpu().numpy()
+        assert layer.sync_status() == EMB_OK
+        # reference: unseen ids contribute nothing (the reserved key stands in for them)
+        keys_ref = keys2.copy()
+        for t, spec in enumerate(w.tables):
+            if spec.dynamic:
+                lo_, hi_ = b.offsets[t * w.batch], b.offsets[(t + 1) * w.batch]
+                seen = np.isin(keys2[lo_:hi_], b.keys[lo_:hi_])
+                keys_ref[lo_:hi_][~seen] = np.iinfo(np.int64).min
+        ref, _ = _dynamic_reference(w, ci.Batch(keys_ref, b.offsets, b.table_ids, w.batch), g, seed)
+        assert max_rel_err(got, ref.out, ref.out_scale) <= 1e-5
+    finally:
+        layer.close()

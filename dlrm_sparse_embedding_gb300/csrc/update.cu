@@ -88,7 +88,10 @@ __device__ __forceinline__ float entry_factor(const ReduceArgs& a, const uint16_
 // with rows wider than 64 run one lane group per warp and gain from more
 // warps in flight (10 blocks, 48 registers); narrower layers lose more to the
 // spills than they gain (8 blocks, 64 registers).
-template <int kMinBlocks>
+// kWindow: chunks of 128 lookups or more load their whole key window once
+// (faster on multi-hot layers, where chunks are long); short chunks find
+// their bounds and keys with direct loads (faster on one-hot layers).
+template <int kMinBlocks, bool kWindow>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(ReduceArgs a)
 {
     extern __shared__ uint32_t smem_runs[];
@@ -101,16 +104,63 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
     uint16_t* epos = reinterpret_cast<uint16_t*>(ebag + cap);
     const uint32_t limit = a.key_limit_dev ? (uint32_t)*a.key_limit_dev : a.key_limit;
 
-    const int64_t p0 = chunk_start(a, chunk, lane);
-    const int64_t p1 = chunk + 1 < a.nchunks ? chunk_start(a, chunk + 1, lane) : a.n;
-    if (p0 >= p1) return;
-    const bool first_before = p0 > 0 && a.skeys[p0] == a.skeys[p0 - 1];
-    const bool last_after = p1 < a.n && a.skeys[p1] == a.skeys[p1 - 1];
+    const int64_t base = chunk * a.chunk;
+    int64_t p0, p1;
+    bool first_before, last_after;
+    if constexpr (kWindow) {
+        // 1. the sorted keys of [base - 1, base + 2C) -- every key the chunk's
+        //    bounds and runs depend on -- in one pass of independent loads, into
+        //    the run list's space (the staging below writes it only behind its
+        //    reads: a run or entry index never exceeds its lookup's offset)
+        const int64_t C = a.chunk, n = a.n;
+        uint32_t* keys_s = runs;   // keys_s[q] = skeys[base - 1 + q]
+        {
+            const int W = (int)((base + 2 * C < n ? base + 2 * C : n) - base + 1);
+#pragma unroll 4
+            for (int q = lane; q < W; q += 32) keys_s[q] = base - 1 + q >= 0 ? a.skeys[base - 1 + q] : 0u;
+        }
+        __syncwarp();
+        // chunk bounds: a nominal start snaps forward to the first run start
+        // within C lookups (or stays when one run covers them all)
+        p0 = 0;
+        p1 = n;
+        for (int side = 0; side < 2; ++side) {
+            const int64_t c = chunk + side;
+            if (c == 0 || c >= a.nchunks) continue;
+            const int64_t b0 = c * C, lim = b0 + C < n ? b0 + C : n;
+            int64_t start = b0;
+            for (int64_t w = b0; w < lim; w += 32) {
+                const int64_t p = w + lane;
+                const bool head = p < lim && keys_s[p - base + 1] != keys_s[p - base];
+                const uint32_t m = __ballot_sync(0xffffffffu, head);
+                if (m) {
+                    start = w + __ffs(m) - 1;
+                    break;
+                }
+            }
+            if (side == 0) p0 = start; else p1 = start;
+        }
+        if (p0 >= p1) return;
+        first_before = p0 > 0 && keys_s[p0 - base + 1] == keys_s[p0 - base];
+        last_after = p1 < n && keys_s[p1 - base + 1] == keys_s[p1 - base];
+        // the chunk's bags, in one pass of independent loads, where the entries go
+#pragma unroll 4
+        for (int64_t p = p0 + lane; p < p1; p += 32) ebag[p - p0] = a.sbags[p];
+        __syncwarp();
+    } else {
+        p0 = chunk_start(a, chunk, lane);
+        p1 = chunk + 1 < a.nchunks ? chunk_start(a, chunk + 1, lane) : a.n;
+        if (p0 >= p1) return;
+        first_before = p0 > 0 && a.skeys[p0] == a.skeys[p0 - 1];
+        last_after = p1 < a.n && a.skeys[p1] == a.skeys[p1 - 1];
+    }
 
-    // 1. stage the chunk as entries -- maximal groups of equal (key, bag); a
+    // 2. stage the chunk as entries -- maximal groups of equal (key, bag); a
     //    run lists its lookups in bag order, so a bag that hits a row several
     //    times forms one entry -- and list the runs as entry ranges.  Entry e
     //    covers offsets [epos[e], epos[e+1]) from p0; p0 always opens a run.
+    //    In place: every read of an iteration comes before its writes, and a
+    //    write's index is at most its lookup's offset from p0.
     int R = 0, E = 0;
     uint32_t prev_k = 0, prev_b = 0;
     for (int64_t w = p0; w < p1; w += 32) {
@@ -118,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
         const bool valid = p < p1;
         uint32_t k = 0, b = 0;
         if (valid) {
-            k = a.skeys[p];
-            b = a.sbags[p];
+            k = kWindow ? runs[p - base + 1] : a.skeys[p];
+            b = kWindow ? ebag[p - p0] : a.sbags[p];
         }
         uint32_t pk = __shfl_up_sync(0xffffffffu, k, 1), pb = __shfl_up_sync(0xffffffffu, b, 1);
         if (lane == 0) {
@@ -163,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
     const uint32_t gmask = Lg == 32 ? 0xffffffffu : (((1u << Lg) - 1u) << (g * Lg));
 
     if (R == 1 && G > 1) {
-        // 2a. the chunk is one run, usually a piece of a hot row: all lane
+        // 3a. the chunk is one run, usually a piece of a hot row: all lane
         //     groups share its entries, then their sums are merged
         const uint32_t key = a.skeys[p0];
         if (key >= limit) return;
@@ -224,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
         return;
     }
 
-    // 2b. lane groups take runs g, g+G, ...: reduce each and apply it
+    // 3b. lane groups take runs g, g+G, ...: reduce each and apply it
     for (int r = g; r < R; r += G) {
         const int e0 = (int)runs[r], e1 = (int)runs[r + 1];
         const uint32_t key = a.skeys[p0 + epos[e0]];
@@ -396,17 +446,11 @@ int launch_reduce_update(const ReduceArgs& a, cudaStream_t st)
     const int64_t threads = a.nchunks * 32;
     const unsigned blocks = (unsigned)((threads + kThreads - 1) / kThreads);
     const size_t smem = sizeof(uint32_t) * (size_t)(kThreads / 32) * (size_t)warp_words(a.chunk);
-    if (a.max_dim > 64) {
-        if (cudaFuncSetAttribute(reduce_update_chunks<10>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return -1;
-        reduce_update_chunks<10><<<blocks, kThreads, smem, st>>>(a);
-    } else {
-        if (cudaFuncSetAttribute(reduce_update_chunks<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return -1;
-        reduce_update_chunks<8><<<blocks, kThreads, smem, st>>>(a);
-    }
+    auto kernel = a.max_dim > 64 ? (a.chunk >= 128 ? reduce_update_chunks<10, true> : reduce_update_chunks<10, false>)
+                                 : (a.chunk >= 128 ? reduce_update_chunks<8, true> : reduce_update_chunks<8, false>);
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return -1;
+    kernel<<<blocks, kThreads, smem, st>>>(a);
     int launched = 1;
     if (a.nchunks > 1) {
         int dev = 0, sms = 152;

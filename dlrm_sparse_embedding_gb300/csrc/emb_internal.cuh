@@ -233,8 +233,9 @@ struct ReduceArgs {
     int64_t ld;
     const float* bag_scale;
     float* slots;               // [nchunks][2][kMaxDim]
-    uint32_t* split_list;       // [nchunks] chunks where a split run starts
-    int* split_count;
+    uint32_t* split_list;       // [nchunks] chunks where a split run starts (short rows from the front,
+                                // rows split over many chunks from the back)
+    int* split_count;           // [4] entries of the two lists, then the combine's work counters
     int32_t max_dim;            // widest table of the layer (selects the chunk kernel's occupancy)
     int* err;
 };

@@ -404,7 +404,7 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
          dalloc_n(L, &L->ukey, L->max_unique) && dalloc_n(L, &L->uslot, L->max_unique) &&
          dalloc_n(L, &L->ukey_s, L->max_unique) && dalloc_n(L, &L->uslot_s, L->max_unique) &&
          dalloc_n(L, &L->bits_dev, 1) && dalloc_n(L, &L->slots, L->nchunks_max * 2 * kMaxDim) &&
-         dalloc_n(L, &L->split_list, L->nchunks_max) && dalloc_n(L, &L->split_count, 1) &&
+         dalloc_n(L, &L->split_list, L->nchunks_max) && dalloc_n(L, &L->split_count, 4) &&
          dalloc_n(L, &L->err, 1) && dalloc_n(L, &L->scratch64, 2) && dalloc_n(L, &L->d_init_acc, num_tables);
     std::vector<int32_t> dyn;
     std::vector<float> init_acc(num_tables);

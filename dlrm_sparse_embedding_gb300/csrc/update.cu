@@ -37,8 +37,10 @@ namespace emb {
 namespace {
 
 constexpr int kThreads = 128;   // chunk kernel block (small blocks recycle as soon as their chunks finish)
-constexpr int kCombineThreads = 256;
-constexpr int kCombineBlocksPerSM = 4;
+constexpr int kCombineThreads = 1024;   // combine block: all warps on a long row, or 4 groups of 256 on short ones
+constexpr int kCombineGroups = 4;
+constexpr int kLongChunks = 512;
+constexpr int kCombineBlocksPerSM = 1;   // one 1024-thread block per SM
 
 __device__ __forceinline__ float* slot_ptr(float* slots, int64_t chunk, int which)
 {
@@ -64,6 +66,26 @@ __device__ __forceinline__ int64_t chunk_start(const ReduceArgs& a, int64_t c, i
         if (m) return w + __ffs(m) - 1;
     }
     return base;
+}
+
+// The key kLongChunks chunks past p1 (the position a split row must still
+// cover to count as long), loaded as soon as the chunk's bounds are known.
+__device__ __forceinline__ uint32_t far_key_of(const ReduceArgs& a, int64_t p1)
+{
+    const int64_t probe = p1 + kLongChunks * a.chunk < a.n ? p1 + kLongChunks * a.chunk : a.n - 1;
+    return a.skeys[probe];
+}
+
+// Registers the split row starting in `chunk` for the combine: a row still
+// present kLongChunks chunks further on (far_key equals its key) goes to the
+// long list, which fills split_list from the back; others to the short list
+// (from the front).  Together they hold at most nchunks entries.
+__device__ __forceinline__ void register_split(const ReduceArgs& a, int64_t chunk, uint32_t far_key, uint32_t key)
+{
+    if (far_key == key)
+        a.split_list[a.nchunks - 1 - atomicAdd(a.split_count + 1, 1)] = (uint32_t)chunk;
+    else
+        a.split_list[atomicAdd(a.split_count, 1)] = (uint32_t)chunk;
 }
 
 // Shared memory per warp, in 32-bit words: run starts [2c+2] (entry
@@ -107,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
     const int64_t base = chunk * a.chunk;
     int64_t p0, p1;
     bool first_before, last_after;
+    uint32_t far_key = 0;   // read only when the last run continues past the chunk
     if constexpr (kWindow) {
         // 1. the sorted keys of [base - 1, base + 2C) -- every key the chunk's
         //    bounds and runs depend on -- in one pass of independent loads, into
@@ -143,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
         if (p0 >= p1) return;
         first_before = p0 > 0 && keys_s[p0 - base + 1] == keys_s[p0 - base];
         last_after = p1 < n && keys_s[p1 - base + 1] == keys_s[p1 - base];
+        if (last_after) far_key = far_key_of(a, p1);
         // the chunk's bags, in one pass of independent loads, where the entries go
 #pragma unroll 4
         for (int64_t p = p0 + lane; p < p1; p += 32) ebag[p - p0] = a.sbags[p];
@@ -153,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
         if (p0 >= p1) return;
         first_before = p0 > 0 && a.skeys[p0] == a.skeys[p0 - 1];
         last_after = p1 < a.n && a.skeys[p1] == a.skeys[p1 - 1];
+        if (last_after) far_key = far_key_of(a, p1);
     }
 
     // 2. stage the chunk as entries -- maximal groups of equal (key, bag); a
@@ -270,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
             const float ssq = tb.opt == EMB_OPT_ROWWISE_ADAGRAD ? group_sum(sq4(gs), Lg, 0xffffffffu) : 0.f;
             if (g == 0 && colok) apply_update4(tb, row, elem, gs, wv, av, ssq, li == 0);
         }
-        if (after && !before && lane == 0) a.split_list[atomicAdd(a.split_count, 1)] = (uint32_t)chunk;
+        if (after && !before && lane == 0) register_split(a, chunk, far_key, key);
         return;
     }
 
@@ -333,44 +358,60 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
             if (colok) apply_update4(tb, row, elem, gs, wv, av, ssq, li == 0);
         }
         // the chunk where a split run starts registers it for the combine kernel
-        if (after && !before && li == 0) a.split_list[atomicAdd(a.split_count, 1)] = (uint32_t)chunk;
+        if (after && !before && li == 0) register_split(a, chunk, far_key, key);
         __syncwarp(gmask);
     }
 }
 
-// Adds the pieces of the split run that crosses boundary c (c*chunk), which
-// starts in chunk c-1, and applies its update.  Whole block: warp w adds
-// pieces w, w+W, w+2W, ... (four loads in flight), then warp 0 adds the warps'
-// sums in warp order.
-__device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int64_t& s_last,
-                                            float (*part)[kMaxDim])
+// Barrier over `nthr` threads (a multiple of 32) on named barrier `bar`,
+// returning how many of them passed pred.
+__device__ __forceinline__ int group_count(int bar, int nthr, bool pred)
 {
-    constexpr int W = kCombineThreads / 32;
+    int r;
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.popc.u32 %0, %2, %3, p;\n\t}"
+                 : "=r"(r) : "r"((int)pred), "r"(bar), "r"(nthr) : "memory");
+    return r;
+}
+
+__device__ __forceinline__ void group_sync(int bar, int nthr)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthr) : "memory");
+}
+
+// Adds the pieces of the split run that crosses boundary c (c*chunk), which
+// starts in chunk c-1, and applies its update.  A group of nthr threads (tid
+// its thread index, warps w0 .. w0 + nthr/32 - 1 of the block, named barrier
+// bar): warp w adds pieces w, w+W, w+2W, ... (four loads in flight), then the
+// group's first warp adds the warps' sums in warp order.
+__device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int64_t& s_last, float (*part)[kMaxDim],
+                                            int bar, int nthr, int tid, int w0)
+{
+    const int W = nthr / 32;
     const int64_t pb = c * a.chunk;
     const uint32_t key = a.skeys[pb];
-    for (int64_t base = c;; base += kCombineThreads) {
-        const int64_t cc = base + threadIdx.x;
+    for (int64_t base = c;; base += nthr) {
+        const int64_t cc = base + tid;
         // chunk cc+1 starts inside the run iff the whole window of its nominal
         // start holds this key (otherwise its start snapped to a later run)
         bool cont = false;
         if (cc + 1 < a.nchunks) {
-            const int64_t w0 = (cc + 1) * a.chunk;
-            const int64_t w1 = w0 + a.chunk < a.n ? w0 + a.chunk : a.n;
-            cont = a.skeys[w0] == key && a.skeys[w1 - 1] == key;
+            const int64_t win0 = (cc + 1) * a.chunk;
+            const int64_t win1 = win0 + a.chunk < a.n ? win0 + a.chunk : a.n;
+            cont = a.skeys[win0] == key && a.skeys[win1 - 1] == key;
         }
-        const int cnt = __syncthreads_count(cont);
-        if (cnt < kCombineThreads) {
-            if (threadIdx.x == 0) s_last = base + cnt;
+        const int cnt = group_count(bar, nthr, cont);
+        if (cnt < nthr) {
+            if (tid == 0) s_last = base + cnt;
             break;
         }
     }
-    __syncthreads();
+    group_sync(bar, nthr);
     const int64_t last = s_last;
     const int64_t P = last - c + 2;   // tail piece of chunk c-1, head pieces of chunks c..last
     const uint32_t bag0 = a.sbags[pb];
     const int t = (int)(bag0 / (uint32_t)a.batch);
     const TableDev tb = a.tables[t];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = tid & 31, warp = tid >> 5;
     const bool colok = 4 * lane < tb.dim;
     float s[4] = {0.f, 0.f, 0.f, 0.f}, cc4[4] = {0.f, 0.f, 0.f, 0.f};
     if (colok) {
@@ -400,15 +441,15 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
             kahan_add(s[3], cc4[3], v.w);
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) part[warp][4 * lane + q] = __fsub_rn(s[q], cc4[q]);
+        for (int q = 0; q < 4; ++q) part[w0 + warp][4 * lane + q] = __fsub_rn(s[q], cc4[q]);
     }
-    __syncthreads();
+    group_sync(bar, nthr);
     if (warp == 0) {
         float gs[4] = {0.f, 0.f, 0.f, 0.f}, gc[4] = {0.f, 0.f, 0.f, 0.f};
         if (colok) {
             for (int w = 0; w < W; ++w) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) kahan_add(gs[q], gc[q], part[w][4 * lane + q]);
+                for (int q = 0; q < 4; ++q) kahan_add(gs[q], gc[q], part[w0 + w][4 * lane + q]);
             }
         }
         float g[4];
@@ -424,17 +465,35 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
     }
 }
 
-
-// Persistent blocks over the runs registered as split: each adds its run's
-// pieces in chunk order and applies the update.
+// Persistent blocks of kCombineThreads over the runs registered as split,
+// taking work from counters (split_count[2] for long rows, [3] for short
+// ones): a block first adds long rows with all its warps, then works as
+// kCombineGroups independent groups (named barriers 1..) on short rows.
 __global__ void __launch_bounds__(kCombineThreads) reduce_update_combine(ReduceArgs a)
 {
-    __shared__ int64_t s_last;
+    __shared__ int64_t s_last[kCombineGroups];
+    __shared__ int s_item[kCombineGroups];
     __shared__ float part[kCombineThreads / 32][kMaxDim];
-    const int nsplit = *a.split_count;
-    for (int item = blockIdx.x; item < nsplit; item += gridDim.x) {
-        combine_run(a, (int64_t)a.split_list[item] + 1, s_last, part);
-        __syncthreads();
+    const int nlong = a.split_count[1], nshort = a.split_count[0];
+    for (;;) {
+        if (threadIdx.x == 0) s_item[0] = atomicAdd(a.split_count + 2, 1);
+        group_sync(0, kCombineThreads);
+        const int item = s_item[0];
+        if (item >= nlong) break;
+        combine_run(a, (int64_t)a.split_list[a.nchunks - 1 - item] + 1, s_last[0], part, 0, kCombineThreads,
+                    threadIdx.x, 0);
+        group_sync(0, kCombineThreads);
+    }
+    constexpr int kGT = kCombineThreads / kCombineGroups;
+    const int g = threadIdx.x / kGT, tid = threadIdx.x % kGT;
+    group_sync(0, kCombineThreads);   // every thread has read s_item[0]
+    for (;;) {
+        if (tid == 0) s_item[g] = atomicAdd(a.split_count + 3, 1);
+        group_sync(1 + g, kGT);
+        const int item = s_item[g];
+        if (item >= nshort) break;
+        combine_run(a, (int64_t)a.split_list[item] + 1, s_last[g], part, 1 + g, kGT, tid, g * (kGT / 32));
+        group_sync(1 + g, kGT);
     }
 }
 }  // namespace
@@ -442,7 +501,7 @@ __global__ void __launch_bounds__(kCombineThreads) reduce_update_combine(ReduceA
 int launch_reduce_update(const ReduceArgs& a, cudaStream_t st)
 {
     if (a.n <= 0 || a.nchunks <= 0) return 0;
-    if (cudaMemsetAsync(a.split_count, 0, sizeof(int), st) != cudaSuccess) return -1;
+    if (cudaMemsetAsync(a.split_count, 0, 4 * sizeof(int), st) != cudaSuccess) return -1;
     const int64_t threads = a.nchunks * 32;
     const unsigned blocks = (unsigned)((threads + kThreads - 1) / kThreads);
     const size_t smem = sizeof(uint32_t) * (size_t)(kThreads / 32) * (size_t)warp_words(a.chunk);

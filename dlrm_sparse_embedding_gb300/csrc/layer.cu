@@ -571,6 +571,9 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
     a.err = L->err;
     if (L->timing) harvest_timing(L);
     int rc = EMB_OK;
+    // a dedup a previous forward left running on the side stream still reads
+    // the ids and resolved rows this forward rewrites
+    if (L->early_pending && cudaStreamWaitEvent(st, L->ev_ready, 0) != cudaSuccess) return EMB_ERR_CUDA;
     if (L->timing) cudaEventRecord(L->ev[0], st);   // the forward phase includes resolving dynamic keys
     if (L->num_dyn > 0 && nnz > 0) {
         // dynamic tables: find or insert every key; the kernels after it read rows
@@ -855,6 +858,8 @@ int emb_forward_infer(emb_layer* L, const int64_t* keys, const int64_t* offsets,
         (nnz > 0 && !keys) || !aligned16(out))
         return EMB_ERR_INVALID_ARG;
     cudaStream_t st = S(stream);
+    // the side stream's dedup may still read the resolved rows rewritten here
+    if (L->early_pending && cudaStreamWaitEvent(st, L->ev_ready, 0) != cudaSuccess) return EMB_ERR_CUDA;
     InferArgs ia;
     ia.keys = keys;
     ia.offsets = offsets;

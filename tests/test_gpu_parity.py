@@ -632,3 +632,46 @@ def test_forward_infer_on_dynamic_tables_skips_unseen_ids():
         assert max_rel_err(got, ref.out, ref.out_scale) <= 1e-5
     finally:
         layer.close()
+
+
+def test_inference_between_forward_and_backward_changes_nothing():
+    # with the dedup running early on the layer's second stream, an inference
+    # forward (which rewrites the dynamic tables' resolved rows) between a
+    # forward and its backward leaves the step bitwise unchanged
+    import torch
+    from dlrm_sparse_embedding_gb300 import EMB_OK, EmbeddingLayer
+    w, b, g = _dynamic_inputs(B=500, seed=41)
+    _, b2, _ = _dynamic_inputs(B=500, seed=42)
+    k, o, tid = (torch.from_numpy(x).cuda() for x in (b.keys, b.offsets, b.table_ids))
+    k2, o2, tid2 = (torch.from_numpy(x).cuda() for x in (b2.keys, b2.offsets, b2.table_ids))
+    grad = torch.from_numpy(g).cuda()
+    res = []
+    for early in (None, "reduction"):
+        layer = EmbeddingLayer(w.tables, w.batch, max(b.nnz, b2.nnz))
+        try:
+            layer.init_uniform(5, w.w_lo, w.w_hi)
+            layer.forward(k2, o2, tid2, w.batch)        # both layers hold the same keys
+            layer.set_early_dedup(early)
+            out = layer.forward(k, o, tid, w.batch).cpu().numpy()
+            if early:
+                layer.forward_infer(k2, o2, tid2, w.batch)
+            layer.backward_update(grad, "reduction")
+            assert layer.sync_status() == EMB_OK
+            rows = []
+            for t, s in enumerate(w.tables):
+                if s.dynamic:   # rows are compared key by key: a key's row depends on insertion order
+                    keys_t = np.unique(np.concatenate([x.keys[x.offsets[t * w.batch]:x.offsets[(t + 1) * w.batch]]
+                                                       for x in (b, b2)]))
+                    r = layer.find_keys(t, torch.from_numpy(keys_t).cuda())
+                    W, A = layer.gather_rows(t, r, with_state=s.opt != "sgd")
+                    W = W.view(torch.int16) if s.dtype == "bf16" else W
+                    rows.append((W.cpu().numpy(), None if A is None else A.cpu().numpy()))
+                else:
+                    rows.append(layer.get_rows(t, 0, s.rows, with_state=s.opt != "sgd"))
+            res.append((out, rows))
+        finally:
+            layer.close()
+    assert np.array_equal(res[0][0], res[1][0])
+    for (wa, sa), (wb, sb) in zip(res[0][1], res[1][1]):
+        assert np.array_equal(wa, wb)
+        assert (sa is None and sb is None) or np.array_equal(sa, sb)

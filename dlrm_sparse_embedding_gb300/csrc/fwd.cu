@@ -72,6 +72,11 @@ __device__ __forceinline__ void kahan_add4(BagStream& st, float4 x)
     kahan_add(st.s.w, st.c.w, x.w);
 }
 
+__device__ __forceinline__ float4 add4(float4 a, float4 b)
+{
+    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;
 
 // Closes (scales and stores) every bag that ends at position `pos`, empty bags included.
@@ -262,20 +267,31 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
                                ? load_cached_row4(tb, kq & ~kCacheBit, li)
                                : load_row4(tb.w, tb.dtype, (int64_t)kq * tb.dim + 4 * li);
             }
-            // rows are added in pairs, then compensated into the bag's sum; a
-            // bag ending inside a pair takes the first row alone
+            // Four rows of one bag are added as a tree ((v0+v1)+(v2+v3)) and
+            // compensated into the bag's sum in one step.  Where a bag ends
+            // inside the four, rows are added in pairs instead, and a bag
+            // ending inside a pair takes the first row alone.
 #pragma unroll
-            for (int u = 0; u < kPrefetch; u += 2) {
-                if (q + u < cnt) {
-                    const bool split = (endbits >> (q + u)) & 1u;
-                    const float4 w1 = split ? make_float4(0.f, 0.f, 0.f, 0.f) : v[u + 1];
-                    kahan_add4(st, make_float4(__fadd_rn(v[u].x, w1.x), __fadd_rn(v[u].y, w1.y),
-                                               __fadd_rn(v[u].z, w1.z), __fadd_rn(v[u].w, w1.w)));
-                    if (split) {
-                        CLOSE_BAGS(base + q + u + 1);
-                        if (q + u + 1 < cnt) kahan_add4(st, v[u + 1]);
+            for (int h = 0; h < kPrefetch; h += 4) {
+                if (q + h >= cnt) continue;
+                const uint32_t eb = endbits >> (q + h);
+                if (q + h + 4 <= cnt && (eb & 7u) == 0) {
+                    kahan_add4(st, add4(add4(v[h], v[h + 1]), add4(v[h + 2], v[h + 3])));
+                    if (eb & 8u) CLOSE_BAGS(base + q + h + 4);
+                    continue;
+                }
+#pragma unroll
+                for (int u = h; u < h + 4; u += 2) {
+                    if (q + u < cnt) {
+                        const bool split = (endbits >> (q + u)) & 1u;
+                        const float4 w1 = split ? make_float4(0.f, 0.f, 0.f, 0.f) : v[u + 1];
+                        kahan_add4(st, add4(v[u], w1));
+                        if (split) {
+                            CLOSE_BAGS(base + q + u + 1);
+                            if (q + u + 1 < cnt) kahan_add4(st, v[u + 1]);
+                        }
+                        if ((endbits >> (q + u + 1)) & 1u) CLOSE_BAGS(base + q + u + 2);
                     }
-                    if ((endbits >> (q + u + 1)) & 1u) CLOSE_BAGS(base + q + u + 2);
                 }
             }
         }

@@ -199,6 +199,21 @@ sort_downsweep(const K* __restrict__ keys_in, const uint32_t* __restrict__ vals_
     const K sub = (c.src_in && key_sub) ? (K)(*key_sub) : (K)0;
     const int64_t base = tile * kTile;
     const uint32_t lt = lanemask_lt();
+    // this thread's digits d0 .. d0+per-1 in the scans below: their totals and
+    // this tile's offsets within them are requested now, so the loads' latency
+    // passes behind the ranking
+    const int per = (nb + kSortThreads - 1) / kSortThreads;   // at most 4 (digits of at most 10 bits)
+    const int d0 = threadIdx.x * per;
+    uint32_t lg_[4], lc_[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        lg_[q] = 0u;
+        lc_[q] = 0u;
+        if (q < per && d0 + q < nb) {
+            lg_[q] = totals[d0 + q];
+            lc_[q] = counts[(int64_t)(d0 + q) * c.ntiles + tile];
+        }
+    }
 
     K k[ITEMS];
     uint32_t v[ITEMS];
@@ -241,27 +256,25 @@ sort_downsweep(const K* __restrict__ keys_in, const uint32_t* __restrict__ vals_
             s += cnt;
         }
         tstart[d] = s;
-        gbase[d] = totals[d];
     }
     __syncthreads();
     // exclusive scans over digits: tile-local starts and global digit bases
     {
-        const int per = (nb + kSortThreads - 1) / kSortThreads;
-        const int d0 = threadIdx.x * per;
         uint32_t st = 0, sg = 0;
-        uint32_t lt_[4], lg_[4];
-        for (int q = 0; q < per && q < 4; ++q) {
-            lt_[q] = (d0 + q < nb) ? tstart[d0 + q] : 0u;
-            lg_[q] = (d0 + q < nb) ? gbase[d0 + q] : 0u;
+        uint32_t lt_[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            lt_[q] = (q < per && d0 + q < nb) ? tstart[d0 + q] : 0u;
             st += lt_[q];
             sg += lg_[q];
         }
         uint32_t ext = block_exclusive_sum(st, wbuf, nullptr);
         uint32_t exg = block_exclusive_sum(sg, wbuf, nullptr);
-        for (int q = 0; q < per && q < 4; ++q) {
-            if (d0 + q < nb) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (q < per && d0 + q < nb) {
                 tstart[d0 + q] = ext;
-                gbase[d0 + q] = exg + counts[(int64_t)(d0 + q) * c.ntiles + tile];
+                gbase[d0 + q] = exg + lc_[q];
             }
             ext += lt_[q];
             exg += lg_[q];

@@ -92,6 +92,28 @@ def algorithmic_bytes(w: ci.Workload, batch: ci.Batch, U_per_table: np.ndarray) 
     return {"forward": fwd, "dedup": dedup, "reduce_update": upd, "step": fwd + dedup + upd}
 
 
+def recorded_traffic(config: str, variant: str, phase: str, root: str = ROOT):
+    """DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of one
+    full-size launch of `phase`'s kernels, from
+    profiles/traffic_<config>_<variant>.json -- or None when there is no
+    record, or when any source file the record names no longer hashes to its
+    recorded SHA-256 (the kernels changed since the counters were taken)."""
+    import hashlib
+    tpath = os.path.join(root, "profiles", "traffic_%s_%s.json" % (config, variant))
+    try:
+        with open(tpath) as f:
+            rec = json.load(f).get(phase)
+        if not rec or not rec.get("sources_sha256"):
+            return None
+        for src, sha in rec["sources_sha256"].items():
+            with open(os.path.join(root, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != sha:
+                    return None
+        return int(rec["traffic_bytes"])
+    except (OSError, ValueError, KeyError, TypeError):
+        return None
+
+
 def unique_per_table(w: ci.Workload, batch: ci.Batch) -> np.ndarray:
     B = w.batch
     U = np.zeros(w.num_tables, dtype=np.int64)
@@ -452,17 +474,7 @@ def main():
     dom_kernel = {"forward": "fwd_pool", "reduce_update": "reduce_update_chunks+combine"}[dom]
     dom_gbs = bytes_[dom] / (per_phase_ms[dom] / 1e3) / 1e9
     step_gbs = bytes_["step"] / (ms / 1e3) / 1e9
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic_%s_%s.json" % (args.config, args.variant))
-    if os.path.exists(tpath) and not (args.batch or args.rows_cap):
-        # ncu DRAM bytes of the dominant phase, valid only while its kernel source is unchanged
-        with open(tpath) as f:
-            rec = json.load(f).get(dom)
-        if rec:
-            import hashlib
-            with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-                if hashlib.sha256(f.read()).hexdigest() == rec["source_sha256"]:
-                    traffic = rec["traffic_bytes"]
+    traffic = None if (args.batch or args.rows_cap) else recorded_traffic(args.config, args.variant, dom)
 
     cpu = None
     if not args.no_cpu_baseline and ws == 1:

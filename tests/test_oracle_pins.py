@@ -275,6 +275,24 @@ def test_forward_matches_torch_embedding_bag_f64(pooling):
 # a4: reduction
 # ---------------------------------------------------------------------------
 
+def test_skipped_lookups_count_in_the_mean_and_pass_no_gradient():
+    # one table of 3 rows x 4, mean pooling, SGD with lr 0.5; bags {0, 7, 2}
+    # (7 is out of range), {} and {-1}.  Values chosen so every result is exact.
+    tables = [_spec(3, 4, "mean", "sgd", lr=0.5)]
+    offsets = np.array([0, 3, 3, 4], np.int64)
+    keys = np.array([0, 7, 2, -1], np.int64)
+    W = np.array([[3, 6, -9, 0], [1, 1, 1, 1], [0, 3, 3, 3]], np.float32)
+    grad = np.array([[3, -3, 6, 0], [5, 5, 5, 5], [7, 7, 7, 7]], np.float32)
+    res = oracle.step(tables, 3, offsets, keys, np.zeros(3, np.int32), grad, _dense_rows([W]))
+    # the mean divides by the whole bag length; empty and all-skipped bags pool to 0
+    assert np.array_equal(res.out, np.array([[1, 3, -2, 1], [0, 0, 0, 0], [0, 0, 0, 0]], np.float32))
+    assert res.n_bad == 2
+    assert res.unique.tolist() == [0, 2] and res.counts.tolist() == [1, 1]
+    # rows 0 and 2 each take bag 0's gradient / 3; the skipped lookups touch no row
+    assert res.rows.row.tolist() == [0, 2] and res.rows.row_start.tolist() == [0, 4]
+    assert np.array_equal(res.W, np.array([2.5, 6.5, -10, 0, -0.5, 3.5, 2, 3], np.float64))
+
+
 @pytest.mark.parametrize("pooling", ["sum", "mean"])
 def test_reduce_broadcasts_to_every_member(pooling):
     # every key distinct: G of each position's row is exactly s_j * grad_out[b]

@@ -32,6 +32,23 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[ctypes.c_void_p]:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, min_numel: Optional[int] = None,
+           shape: Optional[tuple] = None, device: Optional[torch.device] = None) -> None:
+    """Raises ValueError unless `t` is a tensor of `dtype` on `device` holding
+    at least `min_numel` elements, or exactly `shape`.  The C ABI receives bare
+    pointers, so sizes it reads past cannot be checked below this point."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError("%s must be a torch tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError("%s holds %d elements, needs at least %d" % (name, t.numel(), min_numel))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, the batch on %s" % (name, t.device, device))
+
+
 def _spec_field(s, name, default=None):
     v = getattr(s, name, default)
     return v if v is not None else default
@@ -77,6 +94,7 @@ class EmbeddingLayer:
         self.doff = np.concatenate([[0], np.cumsum([int(s.dim) for s in self.tables])[:-1]]).astype(np.int64)
         self.row_base = np.concatenate([[0], np.cumsum([int(s.rows) for s in self.tables])[:-1]]).astype(np.int64)
         self.last_nnz = 0
+        self.last_batch = None   # batch of the last training forward (None: no forward yet)
 
     # -- life cycle ---------------------------------------------------------
     def close(self) -> None:
@@ -95,20 +113,37 @@ class EmbeddingLayer:
         check(lib.emb_init_uniform(self._h, ctypes.c_uint64(seed & (2 ** 64 - 1)), lo, hi, _stream(stream)),
               "emb_init_uniform")
 
+    def _check_batch(self, keys, offsets, table_ids, batch, out):
+        batch = int(batch)
+        bags = len(self.tables) * batch
+        dev = offsets.device if isinstance(offsets, torch.Tensor) else None
+        _check(keys, "keys", torch.int64, device=dev)
+        _check(offsets, "offsets", torch.int64, min_numel=bags + 1)
+        _check(table_ids, "table_ids", torch.int32, min_numel=bags, device=dev)
+        if out is None:
+            out = torch.empty((batch, self.total_dim), dtype=torch.float32, device=dev)
+        _check(out, "out", torch.float32, shape=(batch, self.total_dim), device=dev)
+        return batch, out
+
     def forward(self, keys: torch.Tensor, offsets: torch.Tensor, table_ids: torch.Tensor, batch: int,
                 out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        if out is None:
-            out = torch.empty((batch, self.total_dim), dtype=torch.float32, device=offsets.device)
-        assert keys.dtype == torch.int64 and offsets.dtype == torch.int64 and table_ids.dtype == torch.int32
-        assert out.dtype == torch.float32 and out.shape == (batch, self.total_dim)
+        batch, out = self._check_batch(keys, offsets, table_ids, batch, out)
         nnz = int(keys.numel())
         check(lib.emb_forward(self._h, _ptr(keys) if nnz else None, _ptr(offsets), _ptr(table_ids), nnz,
-                              int(batch), _ptr(out), _stream(stream)), "emb_forward")
+                              batch, _ptr(out), _stream(stream)), "emb_forward")
         self.last_nnz = nnz
+        self.last_batch = batch
         return out
 
     def backward_update(self, grad_out: torch.Tensor, variant: str = "reduction", stream=None) -> None:
-        assert grad_out.dtype == torch.float32
+        """grad_out: fp32 [batch, sum(dim)] of the last forward (extra rows are not read)."""
+        if variant not in VARIANTS:
+            raise ValueError("unknown backward variant %r" % (variant,))
+        _check(grad_out, "grad_out", torch.float32)
+        if self.last_batch is not None:   # before any forward the library reports the state error itself
+            if grad_out.dim() != 2 or grad_out.shape[1] != self.total_dim or grad_out.shape[0] < self.last_batch:
+                raise ValueError("grad_out must be [>= %d, %d], got %s"
+                                 % (self.last_batch, self.total_dim, tuple(grad_out.shape)))
         check(lib.emb_backward_update(self._h, _ptr(grad_out), VARIANTS[variant], _stream(stream)),
               "emb_backward_update")
 
@@ -142,6 +177,7 @@ class EmbeddingLayer:
     # State arrays have state_cols(spec) columns: dim (Adagrad), 1 (row-wise
     # Adagrad); SGD tables have none.
     def gather_rows(self, t: int, rows: torch.Tensor, with_state: bool = False, stream=None):
+        _check(rows, "rows", torch.int64)
         spec = self.tables[t]
         dt = _spec_field(spec, "dtype", "f32")
         n = int(rows.numel())
@@ -174,24 +210,23 @@ class EmbeddingLayer:
     # -- inference ------------------------------------------------------------------
     def cache_build(self, t: int, rows: torch.Tensor, stream=None) -> None:
         """fp16 inference cache of the given rows (int64, device) of table t (empty: none)."""
+        _check(rows, "rows", torch.int64)
         n = int(rows.numel())
         check(lib.emb_cache_build(self._h, t, _ptr(rows) if n else None, n, _stream(stream)), "emb_cache_build")
 
     def forward_infer(self, keys: torch.Tensor, offsets: torch.Tensor, table_ids: torch.Tensor, batch: int,
                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         """Pooled output reading cached rows from the fp16 caches; keeps nothing for a backward."""
-        if out is None:
-            out = torch.empty((batch, self.total_dim), dtype=torch.float32, device=offsets.device)
-        assert keys.dtype == torch.int64 and offsets.dtype == torch.int64 and table_ids.dtype == torch.int32
-        assert out.dtype == torch.float32 and out.shape == (batch, self.total_dim)
+        batch, out = self._check_batch(keys, offsets, table_ids, batch, out)
         nnz = int(keys.numel())
         check(lib.emb_forward_infer(self._h, _ptr(keys) if nnz else None, _ptr(offsets), _ptr(table_ids), nnz,
-                                    int(batch), _ptr(out), _stream(stream)), "emb_forward_infer")
+                                    batch, _ptr(out), _stream(stream)), "emb_forward_infer")
         return out
 
     # -- dynamic tables -----------------------------------------------------------
     def find_keys(self, t: int, keys: torch.Tensor, stream=None) -> torch.Tensor:
         """Rows (int64, -1 when absent) of int64 keys of dynamic table t; inserts nothing."""
+        _check(keys, "keys", torch.int64)
         out = torch.empty(int(keys.numel()), dtype=torch.int64, device=keys.device)
         check(lib.emb_find_keys(self._h, t, _ptr(keys), int(keys.numel()), _ptr(out), _stream(stream)),
               "emb_find_keys")
@@ -199,6 +234,7 @@ class EmbeddingLayer:
 
     # -- fp32 master copies of 16-bit tables ------------------------------------
     def gather_master_rows(self, t: int, rows: torch.Tensor, stream=None) -> torch.Tensor:
+        _check(rows, "rows", torch.int64)
         spec = self.tables[t]
         n = int(rows.numel())
         m = torch.empty((n, int(spec.dim)), dtype=torch.float32, device=rows.device)
@@ -249,7 +285,7 @@ def unique(keys: torch.Tensor, stream=None):
 
     Returns (unique[:U], inverse, counts[:U], seg_offsets[:U+1]); U is read
     back to the host (one synchronisation)."""
-    assert keys.dtype == torch.int64 and keys.is_cuda
+    _check(keys, "keys", torch.int64)
     n = int(keys.numel())
     dev = keys.device
     m = max(n, 1)

@@ -169,6 +169,11 @@ int track(emb_layer* L, int launched)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// p is a multiple of a bytes (a power of two); a null pointer passes, its
+// presence is checked separately.  A device array misaligned for its element
+// type would fault the kernel that reads it, so the host rejects it first.
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
 // ------------------------------- kernels ----------------------------------
 
 __global__ void init_uniform_kernel(void* w, int dtype, int64_t rows, int dim, int t, uint64_t seed, float lo,
@@ -294,6 +299,21 @@ void harvest_timing(emb_layer* L)
 }
 
 }  // namespace
+
+namespace emb {
+
+// Host checks of emb_unique's arguments (shared with emb_unique_noalloc):
+// sizes, presence and the alignment of every array to its element type.
+bool unique_args_valid(const int64_t* keys, int64_t n, const int64_t* unique, const int32_t* inverse,
+                       const int32_t* counts, const int32_t* seg_offsets, const int64_t* num_unique)
+{
+    if (n < 0 || n >= (int64_t(1) << 31) || !num_unique || (n > 0 && (!keys || !unique || !inverse || !counts)))
+        return false;
+    return aligned_to(keys, 8) && aligned_to(unique, 8) && aligned_to(num_unique, 8) && aligned_to(inverse, 4) &&
+           aligned_to(counts, 4) && aligned_to(seg_offsets, 4);
+}
+
+}  // namespace emb
 
 extern "C" {
 
@@ -546,7 +566,8 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
                 int32_t batch, float* out, void* stream)
 {
     if (!L || !offsets || !table_ids || !out || batch < 1 || batch > L->max_batch || nnz < 0 || nnz > L->max_nnz ||
-        (nnz > 0 && !keys) || !aligned16(out))
+        (nnz > 0 && !keys) || !aligned16(out) || !aligned_to(keys, 8) || !aligned_to(offsets, 8) ||
+        !aligned_to(table_ids, 4))
         return EMB_ERR_INVALID_ARG;
     cudaStream_t st = S(stream);
     FwdArgs a;
@@ -710,7 +731,9 @@ int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, vo
 int emb_dedup_result(emb_layer* L, int64_t* unique, int32_t* inverse, int32_t* counts, int32_t* seg_offsets,
                      int32_t* sorted_bags, int64_t* num_unique_host, void* stream)
 {
-    if (!L) return EMB_ERR_INVALID_ARG;
+    if (!L || !aligned_to(unique, 8) || !aligned_to(inverse, 4) || !aligned_to(counts, 4) ||
+        !aligned_to(seg_offsets, 4) || !aligned_to(sorted_bags, 4))
+        return EMB_ERR_INVALID_ARG;
     if (!L->dedup_valid) return EMB_ERR_STATE;
     if (inverse && L->dedup_variant == EMB_BWD_REDUCTION) return EMB_ERR_STATE;
     cudaStream_t st = S(stream);
@@ -749,8 +772,7 @@ int emb_unique_workspace(int64_t n, size_t* bytes)
 int emb_unique(const int64_t* keys, int64_t n, int64_t* unique, int32_t* inverse, int32_t* counts,
                int32_t* seg_offsets, int64_t* num_unique, void* workspace, size_t workspace_bytes, void* stream)
 {
-    if (n < 0 || n >= (int64_t(1) << 31) || !num_unique || (n > 0 && (!keys || !unique || !inverse || !counts)))
-        return EMB_ERR_INVALID_ARG;
+    if (!emb::unique_args_valid(keys, n, unique, inverse, counts, seg_offsets, num_unique)) return EMB_ERR_INVALID_ARG;
     UniqueWs w = unique_ws_layout(n, nullptr);
     if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return EMB_ERR_INVALID_ARG;
@@ -811,7 +833,7 @@ int emb_set_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, const void* w
 
 int emb_cache_build(emb_layer* L, int32_t t, const int64_t* rows, int64_t n, void* stream)
 {
-    if (!L || t < 0 || t >= L->T || n < 0 || n >= (int64_t(1) << 30) || (n > 0 && !rows) ||
+    if (!L || t < 0 || t >= L->T || n < 0 || n >= (int64_t(1) << 30) || (n > 0 && !rows) || !aligned_to(rows, 8) ||
         (n > 0 && L->tabs[t].rows >= (int64_t(1) << 31)))
         return EMB_ERR_INVALID_ARG;
     cudaStream_t st = S(stream);
@@ -855,7 +877,8 @@ int emb_forward_infer(emb_layer* L, const int64_t* keys, const int64_t* offsets,
                       int64_t nnz, int32_t batch, float* out, void* stream)
 {
     if (!L || !offsets || !table_ids || !out || batch < 1 || batch > L->max_batch || nnz < 0 || nnz > L->max_nnz ||
-        (nnz > 0 && !keys) || !aligned16(out))
+        (nnz > 0 && !keys) || !aligned16(out) || !aligned_to(keys, 8) || !aligned_to(offsets, 8) ||
+        !aligned_to(table_ids, 4))
         return EMB_ERR_INVALID_ARG;
     cudaStream_t st = S(stream);
     // the side stream's dedup may still read the resolved rows rewritten here
@@ -895,7 +918,8 @@ int emb_forward_infer(emb_layer* L, const int64_t* keys, const int64_t* offsets,
 
 int emb_find_keys(emb_layer* L, int32_t t, const int64_t* keys, int64_t n, int64_t* rows_out, void* stream)
 {
-    if (!L || t < 0 || t >= L->T || n < 0 || (n > 0 && (!keys || !rows_out)) || !L->tabs[t].dynamic)
+    if (!L || t < 0 || t >= L->T || n < 0 || (n > 0 && (!keys || !rows_out)) || !L->tabs[t].dynamic ||
+        !aligned_to(keys, 8) || !aligned_to(rows_out, 8))
         return EMB_ERR_INVALID_ARG;
     return track(L, launch_dyn_find(L->d_tables, t, keys, n, rows_out, S(stream)));
 }
@@ -928,7 +952,8 @@ int emb_set_master_rows(emb_layer* L, int32_t t, int64_t row0, int64_t n, const 
 
 int emb_gather_master_rows(emb_layer* L, int32_t t, const int64_t* rows, int64_t n, float* master_out, void* stream)
 {
-    if (!L || t < 0 || t >= L->T || n < 0 || (n > 0 && (!rows || !master_out)) || !L->tabs[t].master)
+    if (!L || t < 0 || t >= L->T || n < 0 || (n > 0 && (!rows || !master_out)) || !L->tabs[t].master ||
+        !aligned_to(rows, 8) || !aligned_to(master_out, 4))
         return EMB_ERR_INVALID_ARG;
     if (n == 0) return EMB_OK;
     const TableDev& d = L->tabs[t];
@@ -943,6 +968,8 @@ int emb_gather_rows(emb_layer* L, int32_t t, const int64_t* rows, int64_t n, voi
 {
     if (!L || t < 0 || t >= L->T || n < 0 || (n > 0 && (!rows || !weights_out))) return EMB_ERR_INVALID_ARG;
     const TableDev& d = L->tabs[t];
+    if (!aligned_to(rows, 8) || !aligned_to(weights_out, dtype_bytes(d.dtype)) || !aligned_to(state_out, 4))
+        return EMB_ERR_INVALID_ARG;
     if (state_out && !d.state) return EMB_ERR_INVALID_ARG;
     if (n == 0) return EMB_OK;
     gather_rows_kernel<<<grid_for(n * d.dim, 256), 256, 0, S(stream)>>>(

@@ -45,10 +45,16 @@ int scratch_for_current_device(void** out)
 
 }  // namespace
 
+namespace emb {
+bool unique_args_valid(const int64_t* keys, int64_t n, const int64_t* unique, const int32_t* inverse,
+                       const int32_t* counts, const int32_t* seg_offsets, const int64_t* num_unique);   // layer.cu
+}
+
 extern "C" int emb_unique_noalloc(const int64_t* keys, int64_t n, int64_t* unique, int32_t* inverse,
                                   int32_t* counts, int32_t* seg_offsets, int64_t* num_unique, void* stream)
 {
-    if (n < 0 || n > EMB_UNIQUE_NOALLOC_MAX_KEYS) return EMB_ERR_INVALID_ARG;
+    if (n > EMB_UNIQUE_NOALLOC_MAX_KEYS || !emb::unique_args_valid(keys, n, unique, inverse, counts, seg_offsets, num_unique))
+        return EMB_ERR_INVALID_ARG;
     size_t need = 0;
     if (emb_unique_workspace(n, &need) != EMB_OK || need > kNoAllocScratchBytes) return EMB_ERR_INVALID_ARG;
     void* scratch = nullptr;

@@ -16,7 +16,11 @@
  * recomendacion a escala", section "Integracion del cluster".
  *
  * Conventions shared by every call
- *  - Pointers are DEVICE pointers unless their name ends in _host.
+ *  - Pointers are DEVICE pointers unless their name ends in _host.  Device
+ *    arrays must be aligned to their element size (int64: 8 bytes, int32 and
+ *    fp32: 4, fp16/bf16: 2); the pooled output and grad_out to 16 bytes (the
+ *    kernels move 4 columns at a time).  A misaligned pointer returns
+ *    EMB_ERR_INVALID_ARG with nothing enqueued.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every call that takes a stream only enqueues work on it and
  *    returns without waiting, except the *_host copies and emb_sync_status.

@@ -75,6 +75,34 @@ def test_unique_workspace_is_host_computable(emb):
     assert emb.lib.emb_unique(None, 10, None, None, None, None, None, None, 0, None) == emb.EMB_ERR_INVALID_ARG
 
 
+def _no_cuda_device():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+# The pointers below are addresses no allocation returned.  Each case is
+# rejected by the host checks before any CUDA call; the test still runs only
+# where no GPU is present, so nothing could ever reach a kernel.
+@pytest.mark.skipif(not _no_cuda_device(), reason="host-only check: runs where no GPU is present")
+def test_unique_rejects_misaligned_arrays_on_host(emb):
+    vp = ctypes.c_void_p
+    ws_bytes = emb.unique_workspace_bytes(10)
+    ok = dict(keys=0x10000, uniq=0x20000, inv=0x30000, cnt=0x40000, seg=0x50000, nu=0x60000)
+    for name, bad in [("keys", 0x10004), ("uniq", 0x20004), ("nu", 0x60004), ("inv", 0x30002),
+                      ("cnt", 0x40001), ("seg", 0x50002)]:
+        a = dict(ok, **{name: bad})
+        args = [vp(a["keys"]), 10, vp(a["uniq"]), vp(a["inv"]), vp(a["cnt"]), vp(a["seg"]), vp(a["nu"])]
+        assert emb.lib.emb_unique(*args, vp(0x100000), ws_bytes, None) == emb.EMB_ERR_INVALID_ARG, name
+        assert emb.lib.emb_unique_noalloc(*args, None) == emb.EMB_ERR_INVALID_ARG, name
+    # a workspace that is not 256-byte aligned, or too small
+    args = [vp(ok["keys"]), 10, vp(ok["uniq"]), vp(ok["inv"]), vp(ok["cnt"]), vp(ok["seg"]), vp(ok["nu"])]
+    assert emb.lib.emb_unique(*args, vp(0x100010), ws_bytes, None) == emb.EMB_ERR_INVALID_ARG
+    assert emb.lib.emb_unique(*args, vp(0x100000), ws_bytes - 1, None) == emb.EMB_ERR_INVALID_ARG
+
+
 def test_product_package_does_not_reach_the_oracle():
     pkg = os.path.join(ROOT, "dlrm_sparse_embedding_gb300")
     for dirpath, _, files in os.walk(pkg):

@@ -32,6 +32,24 @@ def test_every_declared_symbol_is_exported(emb):
     assert sorted(emb.EXPORTS) == declared
 
 
+def test_every_declaration_is_documented():
+    # each entry point sits in a group of declarations (with any #define or
+    # enum it needs) directly under a comment: no blank line in between
+    with open(os.path.join(ROOT, "include", "emb.h")) as f:
+        lines = f.read().splitlines()
+    found = 0
+    for i, line in enumerate(lines):
+        m = re.match(r"(?:int|const char\*)\s+(emb_[a-z_0-9]+)\s*\(", line)
+        if not m:
+            continue
+        found += 1
+        j = i - 1
+        while j >= 0 and lines[j].strip() and not lines[j].rstrip().endswith("*/"):
+            j -= 1
+        assert j >= 0 and lines[j].rstrip().endswith("*/"), m.group(1)
+    assert found == len(_declared_symbols())
+
+
 def test_status_strings(emb):
     for s in range(0, -8, -1):
         assert emb.lib.emb_status_string(s)

@@ -1,7 +1,8 @@
 // Inference-only forward with fp16 caches of hot rows.
 //
-// The HugeCTR inference pages (Merlin overview article, HPS / embedding cache)
-// serve lookups from a GPU cache of the frequently used rows.  Here a table
+// The GTC 2022 "Merlin HugeCTR" slides (slide "HUGECTR: SCALABLE, ACCELERATED
+// RECSYS TRAINING") serve inference through an embedding cache on the GPU in
+// front of a hierarchical parameter server (HPS).  Here a table
 // may hold a cache of chosen rows as fp16 copies (half the bytes of an fp32
 // row, so a hot set stays in L2); the inference forward reads a cached row
 // from the cache and every other row from the table.  The cache is a snapshot

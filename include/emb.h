@@ -248,8 +248,10 @@ int emb_get_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n, void* wei
 int emb_set_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n,
                  const void* weights_host, const float* state_host, void* stream);
 
-/* Inference cache of table t (the HPS / embedding-cache idea of the Merlin
- * overview article, section on HugeCTR inference): fp16 copies of n chosen
+/* Inference cache of table t (GTC 2022 HugeCTR slides, slide "HUGECTR:
+ * SCALABLE, ACCELERATED RECSYS TRAINING": inference served through an
+ * embedding cache on the GPU in front of the hierarchical parameter server,
+ * HPS): fp16 copies of n chosen
  * rows (device int64 row ids; a dynamic table's rows from emb_find_keys),
  * looked up through a hash map from row to cache slot.  Replaces any earlier
  * cache of the table; n = 0 removes it.  The copies are a snapshot of the

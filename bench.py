@@ -4,13 +4,20 @@ A step is the whole hot path over one synthetic batch: forward lookup +
 pooling + concatenation, backward dedup, segmented gradient reduction and the
 optimizer update (emb_forward + emb_backward_update through the C ABI).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config dlrm]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config multihot]
                     [--variant reduction|unique_sort|unique_hash] [--impl ours|reference]
 
-Default workload: the DLRM-style one-hot configuration (26 fp32 tables, rows
-log-uniform in [1e3, 1e7], dim 128, batch 65,536, Zipf(1.05) keys, sum
-pooling, Adagrad).  Tables (~29 GB) and the per-step tensors (out and grad_out,
-872 MB each) are far larger than L2, so no L2 flush is needed between steps.
+Default workload: the multi-hot configuration (100 fp32 tables x 1e6 rows x
+dim 64, batch 16,384, per-table hotness U[1,100], Zipf(1.2) keys, mean pooling,
+Adagrad), the largest of the stated workloads in the bytes a step must move.
+Its tables (25.6 GB plus 25.6 GB of Adagrad state) and its per-step tensors
+(keys 0.6 GB, out and grad_out 0.42 GB each) are larger than L2, so no L2
+flush is needed between steps.
+
+Two timed regions of K steps each: the headline one with the library's phase
+timing off, then one with it on (CUDA events around each phase, recorded on
+the stream that runs it, read back only after the region) for the phase
+breakdown and the roofline of the dominant phase.
 
 --impl reference times the CPU oracle (test infrastructure, single-threaded C)
 on a bounded sample of the same workload; it is a reported baseline only.
@@ -20,6 +27,7 @@ rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -71,25 +79,82 @@ def _wbytes(dtype: str) -> int:
     return 4 if dtype == "f32" else 2
 
 
-def algorithmic_bytes(w: ci.Workload, batch: ci.Batch, U_per_table: np.ndarray) -> dict:
-    """Bytes each phase must move through HBM at least once (compulsory)."""
-    T, B, nnz = w.num_tables, w.batch, batch.nnz
-    D = w.total_dim
+def _per_table_bytes(w: ci.Workload, U_per_table: np.ndarray):
+    """Touched-row bytes of the step: rows in their storage type, optimizer
+    state, and what an fp32 master copy adds to the update."""
     rows_bytes = sum(int(U_per_table[t]) * s.dim * _wbytes(s.dtype) for t, s in enumerate(w.tables))
-    # an fp32 master copy: the update reads and writes the master and writes the stored row
+    # an fp32 master copy: the update reads and writes the master (8 B) and
+    # writes the stored row, instead of reading and writing the stored row
     master_bytes = sum(int(U_per_table[t]) * s.dim * (8 - _wbytes(s.dtype))
                        for t, s in enumerate(w.tables) if getattr(s, "master", False))
     state_cols = {"sgd": 0, "adagrad": None, "rowwise_adagrad": 1}
     state_bytes = sum(int(U_per_table[t]) * 4 * (s.dim if state_cols[s.opt] is None else state_cols[s.opt])
                       for t, s in enumerate(w.tables))
-    fwd = 8 * nnz + 8 * (T * B + 1) + 4 * T * B + rows_bytes + 4 * B * D + 8 * nnz   # + gid/bag ids written
-    # dynamic tables: each lookup also reads its map slot and writes and re-reads its resolved row
+    return rows_bytes, master_bytes, state_bytes
+
+
+def algorithmic_bytes(w: ci.Workload, batch: ci.Batch, U_per_table: np.ndarray) -> dict:
+    """Compulsory bytes of each phase: what the method must move through HBM
+    at least once, whatever the implementation.
+
+    forward: keys (8 nnz) + offsets (8 (T B + 1)) + every touched row once +
+    the pooled output (4 B sum(dim)); dedup: keys in (8 nnz), unique ids (8 U),
+    inverse (4 nnz) and counts (4 U) out; reduce+update: grad_out once
+    (4 B sum(dim)), one position per lookup (4 nnz), and every touched row
+    and its optimizer state read and written once.  Dynamic tables add, per
+    lookup, the key's map slot read and its resolved row written and read
+    back (24 B)."""
+    T, B, nnz = w.num_tables, w.batch, batch.nnz
+    D = w.total_dim
+    U = int(np.sum(U_per_table))
+    rows_bytes, master_bytes, state_bytes = _per_table_bytes(w, U_per_table)
+    fwd = 8 * nnz + 8 * (T * B + 1) + rows_bytes + 4 * B * D
     dyn_lookups = sum(int(batch.offsets[(t + 1) * B] - batch.offsets[t * B])
                       for t, s in enumerate(w.tables) if getattr(s, "dynamic", False))
     fwd += 24 * dyn_lookups
-    dedup = 8 * nnz + 8 * nnz                                    # read (id, bag) pairs, write them sorted
-    upd = 4 * B * D + 8 * nnz + 2 * rows_bytes + 2 * state_bytes + master_bytes   # grad once, sorted ids+bags, row/state r+w
+    dedup = 8 * nnz + 8 * U + 4 * nnz + 4 * U
+    upd = 4 * B * D + 4 * nnz + 2 * rows_bytes + 2 * state_bytes + master_bytes
     return {"forward": fwd, "dedup": dedup, "reduce_update": upd, "step": fwd + dedup + upd}
+
+
+def implementation_bytes(w: ci.Workload, batch: ci.Batch, U_per_table: np.ndarray, sort_passes: int) -> dict:
+    """Bytes this implementation moves through HBM by design (each array
+    touched once per pass, no L2 re-reads counted), next to the compulsory
+    bytes: the forward also reads the table ids and writes a 32-bit global id
+    and bag per lookup; the reduction-based dedup sorts those (id, bag) pairs
+    (per pass: the histogram reads the ids, the ranking reads and writes both
+    arrays); the reduction reads the sorted ids and bags."""
+    T, B, nnz = w.num_tables, w.batch, batch.nnz
+    D = w.total_dim
+    rows_bytes, master_bytes, state_bytes = _per_table_bytes(w, U_per_table)
+    comp = algorithmic_bytes(w, batch, U_per_table)
+    fwd = comp["forward"] + 4 * T * B + 8 * nnz
+    dedup = sort_passes * (4 * nnz + 16 * nnz)
+    upd = 4 * B * D + 8 * nnz + 2 * rows_bytes + 2 * state_bytes + master_bytes
+    return {"forward": fwd, "dedup": dedup, "reduce_update": upd, "step": fwd + dedup + upd}
+
+
+def logical_row_bytes(w: ci.Workload, batch: ci.Batch) -> int:
+    """Row bytes the forward reads when every lookup reads its row (one read
+    per lookup): under skewed keys most of them are served by L2."""
+    B = w.batch
+    return sum(int(batch.offsets[(t + 1) * B] - batch.offsets[t * B]) * s.dim * _wbytes(s.dtype)
+               for t, s in enumerate(w.tables))
+
+
+def _bits_for(v: int) -> int:
+    b = 1
+    while b < 64 and (v >> b) != 0:
+        b += 1
+    return b
+
+
+def sort_passes(w: ci.Workload, variant: str) -> int:
+    """Radix-sort passes of the dedup (10-bit digits at most): the global id
+    of the reduction-based and the sort-based variants, which includes the
+    sentinel id one past the last row."""
+    total_rows = sum(s.rows for s in w.tables)
+    return -(-_bits_for(total_rows) // 10)
 
 
 def recorded_traffic(config: str, variant: str, phase: str, root: str = ROOT):
@@ -145,6 +210,13 @@ class ClockSampler:
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # the timed region starts once the sampler is producing samples
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -227,6 +299,18 @@ def oracle_step_timed(w: ci.Workload, batch: ci.Batch, grad: np.ndarray, seed: i
     return time.perf_counter() - t0
 
 
+def lookups_per_sample(w: ci.Workload) -> float:
+    """Mean lookups of one sample (one bag per table) under the workload's hotness law."""
+    h = w.replace(batch=min(w.batch, 4096)).hotness()
+    return float(h.sum()) / h.shape[1]
+
+
+def cpu_sample_batch(w: ci.Workload, target_lookups: int) -> int:
+    """Samples whose lookups come to about target_lookups (at least one, at most the batch)."""
+    n = int(round(target_lookups / max(lookups_per_sample(w), 1.0)))
+    return max(1, min(w.batch, n))
+
+
 def cpu_sample(w: ci.Workload, sample_batch: int):
     ws = w.replace(batch=sample_batch)
     b = ci.make_batch(ws)
@@ -238,7 +322,8 @@ def run_reference(args, w: ci.Workload):
     ws_, rank, _ = _dist()
     if rank != 0:
         return
-    sw, sb, sg = cpu_sample(w, args.cpu_sample_batch)
+    sb_n = cpu_sample_batch(w, args.cpu_sample_lookups)
+    sw, sb, sg = cpu_sample(w, sb_n)
     import oracle
     oracle.build()
     for _ in range(args.warmup):
@@ -246,13 +331,14 @@ def run_reference(args, w: ci.Workload):
     secs = [oracle_step_timed(sw, sb, sg, w.seed) for _ in range(args.steps)]
     per = sum(secs) / len(secs)
     v = sb.nnz / per
-    sample = "%d of %d samples per table (%d lookups), full step a1..a5, %d timed steps" % (
-        args.cpu_sample_batch, w.batch, sb.nnz, args.steps)
+    sample = "%d of the %d samples (%d lookups) per step, full step a1..a5, %d timed steps" % (
+        sb_n, w.batch, sb.nnz, args.steps)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "lookups/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3 * w.batch / args.cpu_sample_batch,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": CONFIG_TEXT[args.config], "batch": w.batch,
+        "data": "synthetic", "config": {"workload": CONFIG_TEXT[args.config], "batch": sb_n, "nnz": int(sb.nnz),
+                                        "sample_of_batch": w.batch,
                                         "variant": "definition (no dedup variant)"},
         "cpu_baseline": {"value": v, "unit": "lookups/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -263,13 +349,14 @@ def run_reference(args, w: ci.Workload):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="dlrm", choices=sorted(CONFIG_TEXT))
+    ap.add_argument("--config", default="multihot", choices=sorted(CONFIG_TEXT))
     ap.add_argument("--variant", default="reduction", choices=["reduction", "unique_sort", "unique_hash"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batches", type=int, default=2, help="distinct seeded batches cycled through")
-    ap.add_argument("--cpu-sample-batch", type=int, default=16384)
+    ap.add_argument("--cpu-sample-lookups", type=int, default=400000,
+                    help="lookups in the oracle's sample of the workload (CPU baseline and reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--early-dedup", action="store_true",
@@ -286,8 +373,7 @@ def main():
     if args.batch:
         w = w.replace(batch=args.batch)
     if args.rows_cap:
-        w = w.replace(tables=tuple(ci.TableSpec(min(t.rows, args.rows_cap), t.dim, t.dtype, t.pooling, t.opt, t.lr,
-                                                t.eps, t.init_acc) for t in w.tables))
+        w = w.replace(tables=tuple(dataclasses.replace(t, rows=min(t.rows, args.rows_cap)) for t in w.tables))
 
     if args.impl == "reference":
         run_reference(args, w)
@@ -338,31 +424,37 @@ def main():
     if status != EMB_OK:
         raise SystemExit("device status %d after warm-up" % status)
 
-    # ---- device-resident timed region ----
-    layer.set_timing(True)
-    layer.phase_times(reset=True)
-    layer.launch_count(reset=True)
+    def timed_region(timing: bool):
+        """Milliseconds per step over K steps (max over ranks), launches, and
+        with timing on the per-phase totals of the library's CUDA events."""
+        layer.set_timing(timing)
+        layer.phase_times(reset=True)
+        layer.launch_count(reset=True)
+        if ws > 1:
+            dist.barrier(device_ids=[local])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(args.steps):
+            step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier(device_ids=[local])
+        ms_ = e0.elapsed_time(e1) / args.steps
+        launches_ = layer.launch_count(reset=True)
+        phases_, nsteps_ = layer.phase_times(reset=True)
+        layer.set_timing(False)
+        return max_over_ranks(ms_, dev), launches_, phases_, nsteps_
+
+    # ---- device-resident timed regions: headline (phase timing off), then phases ----
     clocks = ClockSampler(local)
     if rank == 0:
         clocks.start()
-    if ws > 1:
-        dist.barrier(device_ids=[local])
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(args.steps):
-        step(i)
-    e1.record()
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier(device_ids=[local])
+    ms, launches, _, _ = timed_region(False)
+    ms_phased, _, phases, nsteps = timed_region(True)
     clk = clocks.stop() if rank == 0 else None
-    ms = e0.elapsed_time(e1) / args.steps
-    phases, nsteps = layer.phase_times(reset=True)
-    launches = layer.launch_count(reset=True)
-    layer.set_timing(False)
     status = layer.sync_status()
-    ms = max_over_ranks(ms, dev)
 
     # ---- inference-only forward with fp16 hot-row caches (optional) ----
     infer = None
@@ -470,15 +562,18 @@ def main():
     nnz = batches[0].nnz
     peak, peak_kind = _peaks()
     per_phase_ms = {p: phases[p] / max(nsteps, 1) for p in phases}
-    dom = max(("forward", "reduce_update"), key=lambda p: per_phase_ms[p])
-    dom_kernel = {"forward": "fwd_pool", "reduce_update": "reduce_update_chunks+combine"}[dom]
+    dom = max(("forward", "dedup", "reduce_update"), key=lambda p: per_phase_ms[p])
+    dom_kernel = {"forward": "fwd_pool", "dedup": "sort_upsweep+sort_scan+sort_downsweep (radix sort passes)",
+                  "reduce_update": "reduce_update_chunks+combine"}[dom]
     dom_gbs = bytes_[dom] / (per_phase_ms[dom] / 1e3) / 1e9
     step_gbs = bytes_["step"] / (ms / 1e3) / 1e9
+    impl = implementation_bytes(w, batches[0], U_t, sort_passes(w, args.variant))
     traffic = None if (args.batch or args.rows_cap) else recorded_traffic(args.config, args.variant, dom)
 
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
-        sw, sb, sg = cpu_sample(w, args.cpu_sample_batch)
+        sb_n = cpu_sample_batch(w, args.cpu_sample_lookups)
+        sw, sb, sg = cpu_sample(w, sb_n)
         import oracle
         oracle.build()
         secs = []
@@ -486,8 +581,8 @@ def main():
         while not secs or (time.perf_counter() - t_start < 10.0 and len(secs) < 20):
             secs.append(oracle_step_timed(sw, sb, sg, w.seed))
         cpu = {"value": sb.nnz / (sum(secs) / len(secs)), "unit": "lookups/s", "cores": 1, "kind": "oracle",
-               "sample": "%d of %d samples per table (%d lookups), full step a1..a5, mean of %d runs" % (
-                   args.cpu_sample_batch, w.batch, sb.nnz, len(secs))}
+               "sample": "%d of the %d samples (%d lookups), full step a1..a5, mean of %d runs" % (
+                   sb_n, w.batch, sb.nnz, len(secs))}
 
     line = {
         "metric": METRIC,
@@ -514,10 +609,16 @@ def main():
                                                                        "rowwise_adagrad": 1}[s.opt]
                                      + (4 * s.dim if getattr(s, "master", False) else 0))
                            for s in w.tables) / 1e9, w.batch * w.total_dim * 4 / 1e6),
-                   "parallelism": "replicas x%d" % ws},
+                   "parallelism": "replicas x%d" % ws,
+                   "timing": "headline: %d steps with phase timing off; phases: %d further steps with "
+                             "CUDA events around each phase" % (args.steps, args.steps)},
         "hbm": {"algorithmic_bytes_per_step": bytes_["step"], "achieved_gbs": step_gbs, "peak_gbs": peak,
-                "frac": step_gbs / peak, "peak_kind": peak_kind},
+                "frac": step_gbs / peak, "peak_kind": peak_kind,
+                "algorithmic_bytes_per_phase": {p: bytes_[p] for p in ("forward", "dedup", "reduce_update")},
+                "impl_bytes_per_phase": {p: impl[p] for p in ("forward", "dedup", "reduce_update")},
+                "logical_forward_row_bytes": logical_row_bytes(w, batches[0])},
         "phases_ms": per_phase_ms,
+        "ms_per_step_phase_timing_on": ms_phased,
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": dom_gbs, "peak": peak, "unit": "GB/s",
                      "frac": dom_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes": bytes_[dom], "peak_kind": peak_kind},

@@ -19,7 +19,15 @@ enum : int {
     ERRBIT_TABLE_ID = 2,
     ERRBIT_CAPACITY = 4,
     ERRBIT_TIMEOUT = 8,
+    ERRBIT_OFFSETS = 16,   // offsets outside [0, nnz] or decreasing: clamped, flagged as a bad argument
 };
+
+// Offsets are read clamped into [lo, nnz]: a bad CSR from a caller then never
+// sends a kernel outside the keys or the per-lookup workspace.
+__device__ __forceinline__ int64_t clamp_offset(int64_t v, int64_t lo, int64_t nnz)
+{
+    return v < lo ? lo : (v > nnz ? nnz : v);
+}
 
 constexpr int kMaxDim = 128;          // dims are multiples of 4 in [4, 128]
 constexpr int kMaxTables = 4096;
@@ -245,6 +253,7 @@ int launch_reduce_update(const ReduceArgs& a, cudaStream_t st);   // returns ker
 struct FwdArgs {
     const int64_t* keys;
     const int64_t* offsets;
+    int64_t nnz;                // keys and per-lookup outputs hold nnz entries; offsets are clamped to it
     const int32_t* table_ids;
     int32_t batch;
     int32_t num_tables;
@@ -273,6 +282,7 @@ constexpr unsigned long long kMapEmpty = 0x8000000000000000ull;   // the reserve
 struct DynArgs {
     const int64_t* keys;
     const int64_t* offsets;
+    int64_t nnz;
     int32_t batch;
     const TableDev* tables;
     const int32_t* dyn_tables;  // [num_dyn] indices of the dynamic tables
@@ -307,6 +317,7 @@ int launch_cache_fill(const TableDev& tb, int t, const int64_t* rows, int64_t n,
 struct InferArgs {
     const int64_t* keys;
     const int64_t* offsets;
+    int64_t nnz;
     int32_t batch;
     const TableDev* tables;
     const int32_t* dyn_tables;  // [num_dyn] indices of the dynamic tables

@@ -161,14 +161,26 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
     const int nbg = left <= 0 ? 0 : (left < Lr ? (int)left : Lr);
     if (nbg == 0) return;
     const int64_t j0 = (int64_t)t * B + bg0;
-    const int64_t K0 = __ldg(a.offsets + j0);
+    // offsets are clamped into [0, nnz] and made non-decreasing; a change is flagged
+    const int64_t K0raw = __ldg(a.offsets + j0);
+    const int64_t K0 = clamp_offset(K0raw, 0, a.nnz);
     int64_t my_end = INT64_MAX;
     int my_len = 0;
-    bool my_tid_ok = true;
+    bool my_tid_ok = true, my_bad = false;
     if (li < nbg) {
-        my_end = __ldg(a.offsets + j0 + li + 1);
+        const int64_t raw = __ldg(a.offsets + j0 + li + 1);
+        my_end = clamp_offset(raw, K0, a.nnz);
+        my_bad = my_end != raw;
         my_tid_ok = __ldg(a.table_ids + j0 + li) == t;
     }
+    for (int off = 1; off < Lr; off <<= 1) {
+        const int64_t v = __shfl_up_sync(gmask, my_end, off, Lr);
+        if (li >= off && li < nbg && v > my_end) {
+            my_end = v;
+            my_bad = true;
+        }
+    }
+    if (__any_sync(gmask, my_bad || K0 != K0raw) && li == 0) atomicOr(a.err, ERRBIT_OFFSETS);
     int64_t my_start = __shfl_up_sync(gmask, my_end, 1, Lr);
     if (li == 0) my_start = K0;
     if (li < nbg) {
@@ -316,12 +328,17 @@ __global__ void __launch_bounds__(kThreads) fwd_ids(FwdArgs a)
     const int64_t rows = a.tables[t].rows;
     const uint32_t row_base = a.tables[t].row_base;
     const int64_t* kp = a.tables[t].dynamic ? a.resolved : a.keys;
-    const int64_t K0 = __ldg(a.offsets + j0);
+    // offsets clamped into [0, nnz] and made non-decreasing, as in the pooling kernel
+    const int64_t K0 = clamp_offset(__ldg(a.offsets + j0), 0, a.nnz);
     int64_t my_end = INT64_MAX;
     bool my_tid_ok = true;
     if (lane < nbg) {
-        my_end = __ldg(a.offsets + j0 + lane + 1);
+        my_end = clamp_offset(__ldg(a.offsets + j0 + lane + 1), K0, a.nnz);
         my_tid_ok = __ldg(a.table_ids + j0 + lane) == t;
+    }
+    for (int off = 1; off < 32; off <<= 1) {
+        const int64_t v = __shfl_up_sync(0xffffffffu, my_end, off);
+        if (lane >= off && lane < nbg && v > my_end) my_end = v;
     }
     const int64_t K1 = __shfl_sync(0xffffffffu, my_end, nbg - 1);
     for (int64_t base = K0; base < K1; base += 32) {

@@ -70,7 +70,8 @@ __global__ void infer_resolve(InferArgs a)
 {
     const int t = a.dyn_tables[blockIdx.y];
     const TableDev& tb = a.tables[t];
-    const int64_t p0 = a.offsets[(int64_t)t * a.batch], p1 = a.offsets[(int64_t)(t + 1) * a.batch];
+    const int64_t p0 = clamp_offset(a.offsets[(int64_t)t * a.batch], 0, a.nnz);
+    const int64_t p1 = clamp_offset(a.offsets[(int64_t)(t + 1) * a.batch], p0, a.nnz);
     for (int64_t i = p0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p1;
          i += (int64_t)gridDim.x * blockDim.x) {
         const uint64_t k = (uint64_t)a.keys[i];

@@ -87,10 +87,17 @@ struct emb_layer {
     ReduceArgs early_r{};                 // where that dedup leaves its sorted keys and bags
 
     // phase timing: events around the forward kernel, the dedup and the
-    // reduction, recorded on the streams that run them
+    // reduction, recorded on the streams that run them.  Each step takes the
+    // next slot of a ring, and a slot's events are read when the ring comes
+    // back to it (or at emb_phase_times), so timing adds no host wait per step.
     bool timing = false;
-    cudaEvent_t ev[6] = {};               // fwd start/end, dedup start/end, reduce start/end
-    bool fwd_pending = false, bwd_pending = false;
+    struct TimingSlot {
+        cudaEvent_t ev[6] = {};           // fwd start/end, dedup start/end, reduce start/end
+        bool fwd_pending = false, bwd_pending = false;
+    };
+    static constexpr int kTimingRing = 64;
+    TimingSlot tslot[kTimingRing];
+    int tcur = 0;                         // slot of the latest forward
     double phase_ms[EMB_NUM_PHASES] = {0, 0, 0};
     int64_t timed_steps = 0;
 };
@@ -277,25 +284,40 @@ UniqueWs unique_ws_layout(int64_t n, char* base)
     return w;
 }
 
-// Folds the events of a finished phase pair into the totals (waits for them).
-void harvest_timing(emb_layer* L)
+// Folds the events of one ring slot into the totals (waits for them).
+void harvest_slot(emb_layer* L, emb_layer::TimingSlot& s)
 {
     float ms = 0.f;
-    if (L->fwd_pending) {
-        if (cudaEventSynchronize(L->ev[1]) == cudaSuccess && cudaEventElapsedTime(&ms, L->ev[0], L->ev[1]) == cudaSuccess)
+    if (s.fwd_pending) {
+        if (cudaEventSynchronize(s.ev[1]) == cudaSuccess && cudaEventElapsedTime(&ms, s.ev[0], s.ev[1]) == cudaSuccess)
             L->phase_ms[EMB_PHASE_FORWARD] += ms;
-        L->fwd_pending = false;
+        s.fwd_pending = false;
     }
-    if (L->bwd_pending) {
-        if (cudaEventSynchronize(L->ev[5]) == cudaSuccess) {
-            if (cudaEventElapsedTime(&ms, L->ev[2], L->ev[3]) == cudaSuccess) L->phase_ms[EMB_PHASE_DEDUP] += ms;
-            if (cudaEventElapsedTime(&ms, L->ev[4], L->ev[5]) == cudaSuccess)
+    if (s.bwd_pending) {
+        if (cudaEventSynchronize(s.ev[5]) == cudaSuccess) {
+            if (cudaEventElapsedTime(&ms, s.ev[2], s.ev[3]) == cudaSuccess) L->phase_ms[EMB_PHASE_DEDUP] += ms;
+            if (cudaEventElapsedTime(&ms, s.ev[4], s.ev[5]) == cudaSuccess)
                 L->phase_ms[EMB_PHASE_REDUCE_UPDATE] += ms;
         }
-        L->bwd_pending = false;
+        s.bwd_pending = false;
         L->timed_steps += 1;
     }
     cudaGetLastError();
+}
+
+// Folds every slot still holding events, oldest first.
+void harvest_timing(emb_layer* L)
+{
+    for (int i = 1; i <= emb_layer::kTimingRing; ++i) harvest_slot(L, L->tslot[(L->tcur + i) % emb_layer::kTimingRing]);
+}
+
+// The slot a forward records into: the next one of the ring, its old events read first.
+emb_layer::TimingSlot& next_timing_slot(emb_layer* L)
+{
+    L->tcur = (L->tcur + 1) % emb_layer::kTimingRing;
+    emb_layer::TimingSlot& s = L->tslot[L->tcur];
+    harvest_slot(L, s);
+    return s;
 }
 
 }  // namespace
@@ -467,8 +489,9 @@ int emb_destroy(emb_layer* L)
 {
     if (!L) return EMB_OK;
     cudaDeviceSynchronize();
-    for (cudaEvent_t& e : L->ev)
-        if (e) cudaEventDestroy(e);
+    for (auto& s : L->tslot)
+        for (cudaEvent_t& e : s.ev)
+            if (e) cudaEventDestroy(e);
     if (L->ev_in) cudaEventDestroy(L->ev_in);
     if (L->ev_ready) cudaEventDestroy(L->ev_ready);
     if (L->side) cudaStreamDestroy(L->side);
@@ -573,6 +596,7 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
     FwdArgs a;
     a.keys = keys;
     a.offsets = offsets;
+    a.nnz = nnz;
     a.table_ids = table_ids;
     a.batch = batch;
     a.num_tables = L->T;
@@ -590,17 +614,18 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
     a.infer = false;
     for (const TableDev& d : L->tabs) a.rows16 = a.rows16 && d.dtype != EMB_F32;
     a.err = L->err;
-    if (L->timing) harvest_timing(L);
+    cudaEvent_t* ev = L->timing ? next_timing_slot(L).ev : nullptr;
     int rc = EMB_OK;
     // a dedup a previous forward left running on the side stream still reads
     // the ids and resolved rows this forward rewrites
     if (L->early_pending && cudaStreamWaitEvent(st, L->ev_ready, 0) != cudaSuccess) return EMB_ERR_CUDA;
-    if (L->timing) cudaEventRecord(L->ev[0], st);   // the forward phase includes resolving dynamic keys
+    if (ev) cudaEventRecord(ev[0], st);   // the forward phase includes resolving dynamic keys
     if (L->num_dyn > 0 && nnz > 0) {
         // dynamic tables: find or insert every key; the kernels after it read rows
         DynArgs da;
         da.keys = keys;
         da.offsets = offsets;
+        da.nnz = nnz;
         da.batch = batch;
         da.tables = L->d_tables;
         da.dyn_tables = L->d_dyn_tables;
@@ -620,18 +645,18 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
         a.write_ids = false;
         if (cudaEventRecord(L->ev_in, st) != cudaSuccess || cudaStreamWaitEvent(L->side, L->ev_in, 0) != cudaSuccess)
             return EMB_ERR_CUDA;
-        if (L->timing) cudaEventRecord(L->ev[2], L->side);
+        if (ev) cudaEventRecord(ev[2], L->side);
         rc = track(L, launch_forward_ids(a, L->side));
         L->early_r = ReduceArgs{};
         if (rc == EMB_OK) rc = launch_dedup(L, L->early_variant, nnz, L->side, L->early_r);
-        if (L->timing) cudaEventRecord(L->ev[3], L->side);
+        if (ev) cudaEventRecord(ev[3], L->side);
         if (rc == EMB_OK && cudaEventRecord(L->ev_ready, L->side) != cudaSuccess) rc = EMB_ERR_CUDA;
         if (rc != EMB_OK) return rc;
     }
     rc = track(L, launch_forward(a, st));
-    if (L->timing && rc == EMB_OK) {
-        cudaEventRecord(L->ev[1], st);
-        L->fwd_pending = true;
+    if (ev && rc == EMB_OK) {
+        cudaEventRecord(ev[1], st);
+        L->tslot[L->tcur].fwd_pending = true;
     }
     if (rc != EMB_OK) return rc;
     L->fwd_done = true;
@@ -688,6 +713,12 @@ int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, vo
     r.err = L->err;
     int rc = EMB_OK;
     L->dedup_valid = false;
+    emb_layer::TimingSlot* ts = nullptr;
+    if (L->timing) {
+        ts = &L->tslot[L->tcur];
+        if (ts->bwd_pending) harvest_slot(L, *ts);   // a second backward after one forward
+    }
+    cudaEvent_t* ev = ts ? ts->ev : nullptr;
     if (n == 0) {
         if (cudaMemsetAsync(L->num_unique, 0, sizeof(int64_t), st) != cudaSuccess ||
             cudaMemsetAsync(L->seg_off, 0, sizeof(int32_t), st) != cudaSuccess)
@@ -709,18 +740,18 @@ int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, vo
         r.key_limit_dev = L->early_r.key_limit_dev;
         r.gid_of_key = L->early_r.gid_of_key;
     } else {
-        if (L->timing) cudaEventRecord(L->ev[2], st);
+        if (ev) cudaEventRecord(ev[2], st);
         rc = launch_dedup(L, variant, n, st, r);
-        if (L->timing) cudaEventRecord(L->ev[3], st);
+        if (ev) cudaEventRecord(ev[3], st);
     }
     L->early_pending = false;
-    if (L->timing) cudaEventRecord(L->ev[4], st);
+    if (ev) cudaEventRecord(ev[4], st);
     if (rc == EMB_OK) rc = track(L, launch_reduce_update(r, st));
     if (rc == EMB_OK && variant == EMB_BWD_UNIQUE_HASH)
         rc = track(L, launch_hash_clear(L->htable, L->uslot_s, L->num_unique, n, st));
-    if (L->timing && rc == EMB_OK) {
-        cudaEventRecord(L->ev[5], st);
-        L->bwd_pending = true;
+    if (ev && rc == EMB_OK) {
+        cudaEventRecord(ev[5], st);
+        ts->bwd_pending = true;
     }
     if (rc != EMB_OK) return rc;
     L->dedup_valid = variant != EMB_BWD_REDUCTION || L->keep_dedup;
@@ -886,6 +917,7 @@ int emb_forward_infer(emb_layer* L, const int64_t* keys, const int64_t* offsets,
     InferArgs ia;
     ia.keys = keys;
     ia.offsets = offsets;
+    ia.nnz = nnz;
     ia.batch = batch;
     ia.tables = L->d_tables;
     ia.dyn_tables = L->d_dyn_tables;
@@ -896,6 +928,7 @@ int emb_forward_infer(emb_layer* L, const int64_t* keys, const int64_t* offsets,
     FwdArgs a;
     a.keys = keys;
     a.offsets = offsets;
+    a.nnz = nnz;
     a.table_ids = table_ids;
     a.batch = batch;
     a.num_tables = L->T;
@@ -989,7 +1022,7 @@ int emb_sync_status(emb_layer* L, void* stream)
         return EMB_ERR_CUDA;
     if (bits & ERRBIT_CAPACITY) return EMB_ERR_CAPACITY;
     if (bits & ERRBIT_KEY_RANGE) return EMB_ERR_KEY_RANGE;
-    if (bits & ERRBIT_TABLE_ID) return EMB_ERR_INVALID_ARG;
+    if (bits & (ERRBIT_TABLE_ID | ERRBIT_OFFSETS)) return EMB_ERR_INVALID_ARG;
     if (bits & ERRBIT_TIMEOUT) return EMB_ERR_TIMEOUT;
     return EMB_OK;
 }
@@ -997,9 +1030,10 @@ int emb_sync_status(emb_layer* L, void* stream)
 int emb_set_timing(emb_layer* L, int32_t enable)
 {
     if (!L) return EMB_ERR_INVALID_ARG;
-    if (enable && !L->ev[0]) {
-        for (cudaEvent_t& e : L->ev)
-            if (cudaEventCreate(&e) != cudaSuccess) return EMB_ERR_CUDA;
+    if (enable && !L->tslot[0].ev[0]) {
+        for (auto& s : L->tslot)
+            for (cudaEvent_t& e : s.ev)
+                if (cudaEventCreate(&e) != cudaSuccess) return EMB_ERR_CUDA;
     }
     if (!enable) harvest_timing(L);
     L->timing = enable != 0;

@@ -445,6 +445,7 @@ rle_write(const K* __restrict__ sk, const uint32_t* __restrict__ vals, int64_t n
           int64_t* unique64, uint32_t* unique32, int32_t* seg_off, int32_t* inverse)
 {
     __shared__ uint32_t wbuf[kRleThreads / 32 + 1];
+    if (*num_unique < 0) return;   // the sort behind these keys failed: nothing is written
     const int64_t base = (int64_t)blockIdx.x * kRleTile + (int64_t)threadIdx.x * kRleItems;
     bool h[kRleItems];
     uint32_t c = 0;

@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
     // (the chunk's lookups are sorted, so its tables form one range, usually one table)
     int Lg = 1;
     {
-        const int t_first = (int)(ebag[0] / (uint32_t)a.batch);
-        const int t_last = (int)(ebag[E - 1] / (uint32_t)a.batch);
+        const int t_first = min((int)(ebag[0] / (uint32_t)a.batch), a.num_tables - 1);
+        const int t_last = min((int)(ebag[E - 1] / (uint32_t)a.batch), a.num_tables - 1);
         int maxdim = 4;
         for (int t = t_first; t <= t_last; ++t) maxdim = max(maxdim, a.tables[t].dim);
         while (4 * Lg < maxdim) Lg <<= 1;
@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
         if (key >= limit) return;
         const bool before = first_before, after = last_after;
         const int t = (int)(ebag[0] / (uint32_t)a.batch);
+        if (t >= a.num_tables) return;   // only ids left by a forward whose offsets were flagged
         const TableDev& tb = a.tables[t];
         const uint32_t tB = (uint32_t)t * (uint32_t)a.batch;
         const bool mean = tb.pooling == EMB_POOL_MEAN;
@@ -252,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
         int64_t row = 0, elem = 0;
         if (!before && !after && colok && g == 0) {
             const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
-            row = (int64_t)(gid - tb.row_base);
+            row = (int64_t)gid - (int64_t)tb.row_base;
+            if (row < 0 || row >= tb.rows) return;
             elem = row * tb.dim + 4 * li;
             wv = load_update_w4(tb, elem);
             av = load_state4(tb, row, elem);
@@ -307,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
         const bool before = r == 0 && first_before;
         const bool after = r == R - 1 && last_after;
         const int t = (int)(ebag[e0] / (uint32_t)a.batch);
+        if (t >= a.num_tables) continue;   // only ids left by a forward whose offsets were flagged
         const TableDev& tb = a.tables[t];
         const uint32_t tB = (uint32_t)t * (uint32_t)a.batch;
         const bool mean = tb.pooling == EMB_POOL_MEAN;
@@ -316,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
         int64_t row = 0, elem = 0;
         if (!before && !after && colok) {
             const uint32_t gid = a.gid_of_key ? __ldg(a.gid_of_key + key) : key;
-            row = (int64_t)(gid - tb.row_base);
+            row = (int64_t)gid - (int64_t)tb.row_base;
+            if (row < 0 || row >= tb.rows) continue;
             elem = row * tb.dim + 4 * li;
             wv = load_update_w4(tb, elem);
             av = load_state4(tb, row, elem);
@@ -409,7 +413,7 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
     const int64_t last = s_last;
     const int64_t P = last - c + 2;   // tail piece of chunk c-1, head pieces of chunks c..last
     const uint32_t bag0 = a.sbags[pb];
-    const int t = (int)(bag0 / (uint32_t)a.batch);
+    const int t = min((int)(bag0 / (uint32_t)a.batch), a.num_tables - 1);
     const TableDev tb = a.tables[t];
     const int lane = tid & 31, warp = tid >> 5;
     const bool colok = 4 * lane < tb.dim;
@@ -456,9 +460,10 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
 #pragma unroll
         for (int q = 0; q < 4; ++q) g[q] = __fsub_rn(gs[q], gc[q]);
         const float ssq = tb.opt == EMB_OPT_ROWWISE_ADAGRAD ? group_sum(sq4(g), 32, 0xffffffffu) : 0.f;
-        if (colok) {
-            const uint32_t gid = a.gid_of_key ? a.gid_of_key[key] : key;
-            const int64_t row = (int64_t)(gid - tb.row_base);
+        const uint32_t gid = a.gid_of_key ? a.gid_of_key[key] : key;
+        const int64_t row = (int64_t)gid - (int64_t)tb.row_base;
+        // a row outside its table only comes from ids of a forward whose offsets were flagged
+        if (colok && row >= 0 && row < tb.rows) {
             const int64_t elem = row * tb.dim + 4 * lane;
             apply_update4(tb, row, elem, g, load_update_w4(tb, elem), load_state4(tb, row, elem), ssq, lane == 0);
         }

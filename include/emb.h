@@ -106,7 +106,12 @@ typedef struct {
 
 typedef struct emb_layer emb_layer;   /* opaque; owns tables, optimizer state and workspace */
 
-/* Create a layer of `num_tables` tables (1..4096).  The sum of all rows must be
+/* Create a layer of `num_tables` tables (1..4096).  GTC 2022 HugeCTR slides,
+ * "CHALLENGES OF EMBEDDING LAYER": the tables' memory demand is the first
+ * challenge the slide names (there answered by spreading tables over GPUs),
+ * and lower precision such as FP16 the common answer; here every table (fp32,
+ * fp16 or bf16), its optimizer state and the step's workspace are held in this
+ * one GPU's memory.  The sum of all rows must be
  * below 2^32 - 1.  `max_batch` (>= 1) and `max_nnz` (>= 0, < 2^31) bound every
  * later forward: the workspace for that many bags and lookups is allocated
  * here, once, so the step itself allocates nothing.  Weights are NOT
@@ -116,7 +121,8 @@ typedef struct emb_layer emb_layer;   /* opaque; owns tables, optimizer state an
 int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batch,
                int64_t max_nnz, emb_layer** out);
 
-/* Free everything the layer owns.  Synchronises the device first.  NULL is a no-op. */
+/* Free everything the layer owns.  Synchronises the device first.  NULL is a
+ * no-op.  No passage: library convenience. */
 int emb_destroy(emb_layer* layer);
 
 /* Fill every table with the counter-based uniform values
@@ -127,7 +133,8 @@ int emb_destroy(emb_layer* layer);
  * table's init_acc and every fp32 master to the fp32 value.  A dynamic table
  * is emptied instead (all keys forgotten); its rows get the same kind of
  * values, from this seed/lo/hi, when keys take them.  Asynchronous on
- * `stream`. */
+ * `stream`.  No passage: library convenience (the pages give no
+ * initialisation; this counter-based one lets tests regenerate any row). */
 int emb_init_uniform(emb_layer* layer, uint64_t seed, float lo, float hi, void* stream);
 
 /* Forward: lookup + pooling + concatenation (GTC 2022 HugeCTR slides, "COMMON
@@ -145,13 +152,22 @@ int emb_init_uniform(emb_layer* layer, uint64_t seed, float lo, float hi, void* 
  * call.  The lookup's global row ids and bag ids are kept in the layer's
  * workspace for the next emb_backward_update.  A key outside [0, rows_t) or a
  * wrong table id is skipped (contributes 0, gets no gradient) and flagged
- * (EMB_ERR_KEY_RANGE / EMB_ERR_INVALID_ARG at emb_sync_status).  The offsets
- * are trusted: they must be a valid CSR of nnz entries. */
+ * (EMB_ERR_KEY_RANGE / EMB_ERR_INVALID_ARG at emb_sync_status).  Offsets
+ * that leave [0, nnz] or decrease are clamped on the GPU (into [0, nnz],
+ * then to the bag start) before any key is read, and flagged as
+ * EMB_ERR_INVALID_ARG at emb_sync_status; the pooled output and a following
+ * backward are then meaningless but every access stays inside the caller's
+ * arrays and the layer's workspace. */
 int emb_forward(emb_layer* layer, const int64_t* keys, const int64_t* offsets,
                 const int32_t* table_ids, int64_t nnz, int32_t batch, float* out,
                 void* stream);
 
-/* Backward + update for the most recent emb_forward on this layer:
+/* Backward + update for the most recent emb_forward on this layer: the
+ * reduction-based (RB) or unique-based (UB) backward of "NVIDIA EMBark
+ * revoluciona la formacion en sistemas de recomendacion a escala", section
+ * "Integracion del cluster" (RB reduces the gradients of equal keys; UB
+ * dedups the keys first), with the FP32 optimizer of the GTC 2022 HugeCTR
+ * slides, "WEIGHT CONVERSION FOR MIXED PRECISION TRAINING":
  *   G_u[c] = sum over lookups i of row u of s_bag(i) * grad_out[b(i), doff_t + c]
  * then one optimizer step per touched row u (untouched rows are not read):
  *   SGD:     W <- W - lr*G
@@ -177,12 +193,16 @@ int emb_backward_update(emb_layer* layer, const float* grad_out, int32_t variant
  * the same variant, goes straight to the segmented reduction (with another
  * variant it redoes the dedup).  Results are identical to the default mode.
  * variant = -1 (default) turns it off.  The caller's input buffers must stay
- * valid until that backward is enqueued; no extra memory is used. */
+ * valid until that backward is enqueued; no extra memory is used.  Passage:
+ * "NVIDIA EMBark ...", section "Integracion del cluster" (the UB dedup needs
+ * only the keys), and the fused embedding kernels of the GTC 2022 HugeCTR
+ * slides, "HUGECTR EMBEDDING LAYER". */
 int emb_set_early_dedup(emb_layer* layer, int32_t variant);
 
 /* Keep (1) or drop (0, default) the dedup by-products of later backwards so
  * emb_dedup_result can return them.  EMB_BWD_REDUCTION then also writes the
- * sorted unique ids, counts and segment offsets it otherwise never forms. */
+ * sorted unique ids, counts and segment offsets it otherwise never forms.
+ * No passage: library convenience (tests and callers that want the dedup). */
 int emb_set_keep_dedup(emb_layer* layer, int32_t keep);
 
 /* Copy the dedup result of the last emb_backward_update (with keep_dedup on)
@@ -196,12 +216,17 @@ int emb_set_keep_dedup(emb_layer* layer, int32_t keep);
  *   sorted_bags  int32[nnz]  bag id of each lookup, grouped by unique row,
  *                            ascending lookup order inside a group
  *   num_unique_host          U (the call synchronises `stream` for it)
- * EMB_ERR_STATE if there is no such result. */
+ * EMB_ERR_STATE if there is no such result.  Passage: "NVIDIA EMBark ...",
+ * section "Integracion del cluster" (the unique keys, inverse index and
+ * counts of the UB dedup). */
 int emb_dedup_result(emb_layer* layer, int64_t* unique, int32_t* inverse, int32_t* counts,
                      int32_t* seg_offsets, int32_t* sorted_bags, int64_t* num_unique_host,
                      void* stream);
 
-/* Stand-alone dedup of arbitrary int64 keys (the unique-based dedup step):
+/* Stand-alone dedup of arbitrary int64 keys: the dedup step that the
+ * unique-based (UB) backward of "NVIDIA EMBark revoluciona la formacion en
+ * sistemas de recomendacion a escala", section "Integracion del cluster",
+ * runs before reducing gradients:
  *   unique       int64[n]    distinct keys, ascending, in unique[0..U)
  *   inverse      int32[n]    unique[inverse[i]] == keys[i]
  *   counts       int32[n]    counts[k] = #{i : keys[i] == unique[k]}, k < U
@@ -233,7 +258,9 @@ int emb_unique(const int64_t* keys, int64_t n, int64_t* unique, int32_t* inverse
  * make that first call before any stream capture.  All calls share the one
  * array: calls whose GPU work overlaps -- on different streams or from
  * different threads without ordering -- race on it and give wrong results; the
- * contents left by the previous call are never relied on. */
+ * contents left by the previous call are never relied on.  The address looked
+ * up on a device stays in use for the life of the process: after
+ * cudaDeviceReset on that device the function must not be called again. */
 #define EMB_UNIQUE_NOALLOC_MAX_KEYS 262144
 int emb_unique_noalloc(const int64_t* keys, int64_t n, int64_t* unique, int32_t* inverse,
                        int32_t* counts, int32_t* seg_offsets, int64_t* num_unique, void* stream);
@@ -242,7 +269,7 @@ int emb_unique_noalloc(const int64_t* keys, int64_t n, int64_t* unique, int32_t*
  * weights_host holds n*dim values of the table dtype (fp32, or the raw 16-bit
  * patterns of fp16/bf16); state_host (nullable; Adagrad tables only) n*dim
  * fp32, or n fp32 for row-wise Adagrad.  Synchronous: the call waits for
- * `stream`. */
+ * `stream`.  No passage: library convenience (checkpoint and resume, tests). */
 int emb_get_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n, void* weights_host,
                  float* state_host, void* stream);
 int emb_set_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n,
@@ -268,14 +295,16 @@ int emb_cache_build(emb_layer* layer, int32_t t, const int64_t* rows, int64_t n,
  * Dynamic tables look keys up without inserting; an id the table does not
  * hold contributes nothing and is not an error.  Nothing is kept for a
  * backward: a following emb_backward_update still refers to the last
- * emb_forward.  Allocates nothing. */
+ * emb_forward.  Allocates nothing.  Passage: as for emb_cache_build. */
 int emb_forward_infer(emb_layer* layer, const int64_t* keys, const int64_t* offsets,
                       const int32_t* table_ids, int64_t nnz, int32_t batch, float* out,
                       void* stream);
 
 /* Rows of n keys (device int64) of dynamic table t, into rows_out (device
  * int64; -1 for a key the table does not hold).  Inserts nothing.
- * Asynchronous; EMB_ERR_INVALID_ARG for a table that is not dynamic. */
+ * Asynchronous; EMB_ERR_INVALID_ARG for a table that is not dynamic.
+ * Passage: GTC 2022 HugeCTR slides, "HUGECTR EMBEDDING LAYER" (the GPU hash
+ * table from keys to embedding rows). */
 int emb_find_keys(emb_layer* layer, int32_t t, const int64_t* keys, int64_t n, int64_t* rows_out,
                   void* stream);
 
@@ -283,30 +312,34 @@ int emb_find_keys(emb_layer* layer, int32_t t, const int64_t* keys, int64_t n, i
  * with master_fp32 = 1; EMB_ERR_INVALID_ARG otherwise), n*dim fp32 in host
  * memory, for checkpoints and tests.  Synchronous: the call waits for
  * `stream`.  Setting the master does not touch the 16-bit weights: set both
- * (emb_set_rows) to restore a checkpoint. */
+ * (emb_set_rows) to restore a checkpoint.  Passage: GTC 2022 HugeCTR slides,
+ * "WEIGHT CONVERSION FOR MIXED PRECISION TRAINING" (the FP32 weights behind
+ * FP16 tables). */
 int emb_get_master_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n, float* master_host,
                         void* stream);
 int emb_set_master_rows(emb_layer* layer, int32_t t, int64_t row0, int64_t n,
                         const float* master_host, void* stream);
 /* Gather n arbitrary rows' master values (device int64 ids) into a device
  * buffer of n*dim fp32.  Asynchronous; out-of-range ids are skipped and
- * flagged like bad keys. */
+ * flagged like bad keys.  Passage: as for emb_get_master_rows. */
 int emb_gather_master_rows(emb_layer* layer, int32_t t, const int64_t* rows, int64_t n, float* master_out,
                            void* stream);
 
 /* Gather n arbitrary rows (device int64 ids, each in [0, rows_t)) of table t
  * into device buffers: weights_out n*dim of the table dtype, state_out
- * (nullable) n*dim fp32 (row-wise Adagrad: n fp32).  Asynchronous.  Out-of-range ids are skipped and
- * flagged like bad keys. */
+ * (nullable) n*dim fp32 (row-wise Adagrad: n fp32).  Asynchronous.
+ * Out-of-range ids are skipped and flagged like bad keys.  No passage:
+ * library convenience (tests and checkpoints). */
 int emb_gather_rows(emb_layer* layer, int32_t t, const int64_t* rows, int64_t n,
                     void* weights_out, float* state_out, void* stream);
 
 /* Wait for `stream`, then return and clear the sticky device error word
- * (EMB_OK if the GPU saw nothing wrong). */
+ * (EMB_OK if the GPU saw nothing wrong).  No passage: library convenience. */
 int emb_sync_status(emb_layer* layer, void* stream);
 
 /* Number of kernels the library launched on behalf of this layer since the
- * last reset (reset = 1 clears it after reading). */
+ * last reset (reset = 1 clears it after reading).  No passage: library
+ * convenience (measurement). */
 int emb_launch_count(emb_layer* layer, int64_t* count_host, int32_t reset);
 
 /* Phase timing.  With enable = 1 the layer records CUDA events on the call's
@@ -315,14 +348,17 @@ int emb_launch_count(emb_layer* layer, int64_t* count_host, int32_t reset);
  * dedup, from the start of emb_backward_update up to the reduction) and
  * EMB_PHASE_REDUCE_UPDATE (segmented reduction + optimizer kernels) -- and
  * adds their elapsed times.  With early dedup the dedup phase runs on the
- * layer's internal stream, overlapping the forward.  emb_phase_times waits for the last recorded
- * events, writes the accumulated milliseconds of the n (<= 3) phases and the
- * number of steps they cover, and, with reset = 1, clears them. */
+ * layer's internal stream, overlapping the forward.  A step's events are
+ * read back only when a ring of 64 steps comes round to its slot again, so
+ * timing adds no host wait to a step.  emb_phase_times waits for the last
+ * recorded events, writes the accumulated milliseconds of the n (<= 3)
+ * phases and the number of steps they cover, and, with reset = 1, clears
+ * them.  No passage: library convenience (measurement). */
 enum { EMB_PHASE_FORWARD = 0, EMB_PHASE_DEDUP = 1, EMB_PHASE_REDUCE_UPDATE = 2, EMB_NUM_PHASES = 3 };
 int emb_set_timing(emb_layer* layer, int32_t enable);
 int emb_phase_times(emb_layer* layer, float* ms_host, int32_t n, int64_t* steps_host, int32_t reset);
 
-/* Static description of an emb_status value. */
+/* Static description of an emb_status value.  No passage: library convenience. */
 const char* emb_status_string(int status);
 
 #ifdef __cplusplus

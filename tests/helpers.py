@@ -40,6 +40,33 @@ def max_rel_err(got, ref, scale) -> float:
     return float(np.max(diff / den))
 
 
+def plain_rel_err(got, ref, rms_frac: float = 1e-3) -> float:
+    """Plain maximum relative error |gpu - ref| / |ref| over the elements with
+    |ref| >= rms_frac * rms(ref): the companion of max_rel_err that no floor
+    softens, reported beside it.  0 when no element qualifies."""
+    got = np.asarray(got, dtype=np.float64).reshape(-1)
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1)
+    if ref.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    sel = np.abs(ref) >= rms_frac * rms
+    sel &= ref != 0
+    if not np.any(sel):
+        return 0.0
+    return float(np.max(np.abs(got[sel] - ref[sel]) / np.abs(ref[sel])))
+
+
+# (case, quantity, plain max relative error) of every GPU parity comparison in
+# this session; conftest prints them at the end of the run
+PLAIN_REPORT = []
+
+
+def report_plain(case: str, quantity: str, got, ref) -> float:
+    v = plain_rel_err(got, ref)
+    PLAIN_REPORT.append((case, quantity, v))
+    return v
+
+
 def init_rows_fn(w: ci.Workload, seed: int):
     return lambda t, r: ci.init_values(seed, t, r, w.tables[t].dim, w.w_lo, w.w_hi, w.tables[t].dtype)
 
@@ -66,12 +93,16 @@ class GpuStep:
 
 
 def run_gpu_step(w: ci.Workload, batch: ci.Batch, grad: np.ndarray, variant: str, seed: int = 0,
-                 keep_layer: bool = False, max_nnz: Optional[int] = None) -> GpuStep:
+                 keep_layer: bool = False, max_nnz: Optional[int] = None, early: bool = False) -> GpuStep:
+    """One step through the C ABI.  early: the dedup of `variant` runs inside
+    the forward, on the layer's second stream."""
     import torch
     from dlrm_sparse_embedding_gb300 import EmbeddingLayer
     dev = torch.device("cuda", 0)
     layer = EmbeddingLayer(w.tables, w.batch, max(batch.nnz, 1) if max_nnz is None else max_nnz)
     layer.init_uniform(seed, w.w_lo, w.w_hi)
+    if early:
+        layer.set_early_dedup(variant)
     keys = torch.from_numpy(batch.keys).to(dev)
     offsets = torch.from_numpy(batch.offsets).to(dev)
     tids = torch.from_numpy(batch.table_ids).to(dev)

@@ -31,17 +31,45 @@ def test_unique_rows_per_table():
 
 
 def test_algorithmic_bytes_hand_count():
+    """The compulsory bytes of each phase, counted by hand for the two-table case."""
     w, batch = _two_table_case()
     got = bench.algorithmic_bytes(w, batch, bench.unique_per_table(w, batch))
-    nnz, bags, out = 12, 6, 3 * 12 * 4          # out / grad_out: B x sum(dim) fp32
+    nnz, bags, U, out = 12, 6, 6, 3 * 12 * 4    # out / grad_out: B x sum(dim) fp32
     rows = 4 * 8 * 4 + 2 * 4 * 2                # touched rows once, in their storage type
-    fwd = 8 * nnz + 8 * (bags + 1) + 4 * bags + rows + out + 8 * nnz
-    dedup = 16 * nnz                            # (id, bag) pairs read and written sorted
+    fwd = 8 * nnz + 8 * (bags + 1) + rows + out
+    dedup = 8 * nnz + 8 * U + 4 * nnz + 4 * U   # keys in; unique ids, inverse, counts out
     state = 4 * 8 * 4                           # Adagrad accumulators of table 0's touched rows
     master = 2 * 4 * 6                          # table 1: master read + written (8 B) minus the fp16 read (2 B)
-    upd = out + 8 * nnz + 2 * rows + 2 * state + master
+    upd = out + 4 * nnz + 2 * rows + 2 * state + master
     assert got == {"forward": fwd, "dedup": dedup, "reduce_update": upd, "step": fwd + dedup + upd}
-    assert (fwd, dedup, upd) == (560, 192, 832)
+    assert (fwd, dedup, upd) == (440, 216, 784)
+
+
+def test_implementation_bytes_hand_count():
+    """What this implementation moves by design: table ids and 32-bit (id, bag)
+    pairs from the forward, 20 B per element and sort pass, sorted pairs read
+    by the reduction."""
+    w, batch = _two_table_case()
+    got = bench.implementation_bytes(w, batch, bench.unique_per_table(w, batch), sort_passes=2)
+    assert got["forward"] == 440 + 4 * 6 + 8 * 12
+    assert got["dedup"] == 2 * 20 * 12
+    assert got["reduce_update"] == 784 + 4 * 12
+    assert got["step"] == got["forward"] + got["dedup"] + got["reduce_update"]
+
+
+def test_cpu_sample_is_bounded_by_lookups():
+    w = ci.workload("multihot")
+    per = bench.lookups_per_sample(w)
+    assert 100 * 1 <= per <= 100 * 100
+    n = bench.cpu_sample_batch(w, 400000)
+    assert abs(n * per - 400000) <= per
+    assert bench.cpu_sample_batch(ci.workload("tiny"), 10 ** 9) == 256
+    assert bench.cpu_sample_batch(ci.workload("tiny"), 1) == 1
+
+
+def test_logical_row_bytes():
+    w, batch = _two_table_case()
+    assert bench.logical_row_bytes(w, batch) == 6 * 8 * 4 + 6 * 4 * 2
 
 
 def _write_record(root, text, sha=None):

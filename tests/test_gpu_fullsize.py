@@ -17,7 +17,7 @@ import pytest
 
 import ctr_inputs as ci
 import oracle
-from helpers import TOL, gather_rows, max_rel_err, ref_state
+from helpers import TOL, gather_rows, max_rel_err, ref_state, report_plain
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -45,7 +45,10 @@ def _built():
     _CACHE.clear()
 
 
-CASES = [("dlrm", "reduction"), ("dlrm", "unique_hash"), ("dlrm_rowwise", "reduction"), ("huge_master", "reduction"), ("multihot", "reduction"), ("huge", "reduction"),
+# grouped by workload, so each workload's inputs are generated once
+CASES = [("dlrm", "reduction"), ("dlrm", "unique_hash"), ("dlrm_rowwise", "reduction"), ("huge_master", "reduction"),
+         ("multihot", "reduction"), ("multihot", "unique_sort"), ("multihot", "unique_hash"),
+         ("huge", "reduction"), ("huge", "unique_hash"),
          ("skew", "reduction"), ("skew", "unique_sort"), ("skew", "unique_hash")]
 
 
@@ -85,6 +88,7 @@ def test_fullsize_sampled_parity(name, variant):
         full_inv[pos] = inv_s
         ref_out, ref_scale = oracle.forward(w.tables, B, batch.offsets, full_inv, store, bags=bags, want_scale=True)
         assert max_rel_err(out_s, ref_out[bsample], ref_scale[bsample]) <= 1e-5
+        report_plain("%s/%s full size" % (name, variant), "forward", out_s, ref_out[bsample])
 
         # ---- dedup: properties that fix the result uniquely ----
         valid = gids >= 0
@@ -131,6 +135,7 @@ def test_fullsize_sampled_parity(name, variant):
             gw, ga = gather_rows(layer, w, t, st.row[sel])
             idx = st.row_start[sel][:, None] + np.arange(spec.dim)[None, :]
             assert max_rel_err(gw, W[idx], Ws[idx]) <= TOL[spec.dtype], (name, variant, t)
+            report_plain("%s/%s full size" % (name, variant), "weights_" + spec.dtype, gw, W[idx])
             if spec.master:
                 gm = layer.gather_master_rows(t, torch.from_numpy(np.ascontiguousarray(st.row[sel])).cuda())
                 assert max_rel_err(gm.cpu().numpy(), M[idx], Ws[idx]) <= 1e-5, (name, variant, t)

@@ -14,7 +14,7 @@ import pytest
 import ctr_inputs as ci
 import oracle
 from helpers import (TOL, bag_of_positions, expected_sorted_bags, gather_rows, init_rows_fn, max_rel_err,
-                     ref_state, run_gpu_step)
+                     ref_state, report_plain, run_gpu_step)
 
 pytestmark = pytest.mark.gpu
 
@@ -50,14 +50,16 @@ def _small(name):
     raise KeyError(name)
 
 
-def check_step(w, batch, grad, variant, seed=0, expect_status=0, sample_untouched=64):
-    g = run_gpu_step(w, batch, grad, variant, seed, keep_layer=True)
+def check_step(w, batch, grad, variant, seed=0, expect_status=0, sample_untouched=64, early=False):
+    g = run_gpu_step(w, batch, grad, variant, seed, keep_layer=True, early=early)
     layer = g.layer
+    case = "%s/%s%s" % (w.name, variant, "/early" if early else "")
     try:
         assert g.status_fwd == expect_status and g.status_bwd == 0
         ref = oracle.step(w.tables, w.batch, batch.offsets, batch.keys, batch.table_ids, grad, init_rows_fn(w, seed))
         # a1 forward
         assert max_rel_err(g.out, ref.out, ref.out_scale) <= 1e-5
+        report_plain(case, "forward", g.out, ref.out)
         # a3 dedup: bit-exact
         assert np.array_equal(g.unique, ref.unique)
         assert np.array_equal(g.counts, ref.counts)
@@ -74,9 +76,11 @@ def check_step(w, batch, grad, variant, seed=0, expect_status=0, sample_untouche
             W, A = gather_rows(layer, w, t, ref.rows.row[sel])
             idx = (ref.rows.row_start[sel][:, None] + np.arange(spec.dim)[None, :])
             assert max_rel_err(W, ref.W[idx], ref.W_scale[idx]) <= TOL[spec.dtype], (t, spec)
+            report_plain(case, "weights_" + spec.dtype, W, ref.W[idx])
             if spec.opt != "sgd":
                 ra, rs = ref_state(spec, ref.A, ref.A_scale, idx)
                 assert max_rel_err(A, ra, rs) <= 1e-5, t
+                report_plain(case, "state", A, ra)
         # untouched rows keep their initial values exactly
         rng = np.random.default_rng(1)
         for t, spec in enumerate(w.tables):
@@ -104,6 +108,17 @@ def test_step_parity(name, variant):
     batch = ci.make_batch(w)
     grad = ci.make_grad(w)
     check_step(w, batch, grad, variant)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["tiny", "multihot_small", "skew_small"])
+def test_early_dedup_step_parity(name, variant):
+    """The dedup run inside the forward (on the layer's second stream) against
+    the oracle, element by element, like the default mode."""
+    w = _small(name)
+    batch = ci.make_batch(w)
+    grad = ci.make_grad(w)
+    check_step(w, batch, grad, variant, early=True)
 
 
 def test_init_matches_counter_generator_bit_exactly():
@@ -245,6 +260,41 @@ def test_wrong_table_id_is_reported():
         assert layer.sync_status() == EMB_ERR_INVALID_ARG
         ref = oracle.step(tabs, 64, b.offsets, b.keys, b.table_ids, g, init_rows_fn(w, 0))
         assert max_rel_err(out.cpu().numpy(), ref.out, ref.out_scale) <= 1e-5
+    finally:
+        layer.close()
+
+
+@pytest.mark.parametrize("hot", [1, 7])
+def test_bad_offsets_are_clamped_and_reported(hot):
+    """Offsets past nnz or decreasing are clamped on the GPU and reported as a
+    bad argument; the layer stays usable.  A valid step runs first, so every
+    id the backward reads afterwards is one a forward wrote."""
+    import torch
+    from dlrm_sparse_embedding_gb300 import EMB_ERR_INVALID_ARG, EMB_OK, EmbeddingLayer
+    tabs = [ci.TableSpec(100, 16), ci.TableSpec(40, 64)]
+    B = 64
+    w, b, g = _custom(tabs, B, np.full(2 * B, hot), lambda rng, t, s, L: rng.integers(0, s.rows, L))
+    dev = torch.device("cuda", 0)
+    keys, tids, grad = (torch.from_numpy(x).to(dev) for x in (b.keys, b.table_ids, g))
+    good = torch.from_numpy(b.offsets).to(dev)
+    bad_np = b.offsets.copy()
+    bad_np[10] = b.nnz + 1000          # past the end of the keys
+    bad_np[40] = bad_np[39] - 2        # decreasing
+    bad_np[B + 3] = -5                 # negative
+    bad = torch.from_numpy(bad_np).to(dev)
+    layer = EmbeddingLayer(tabs, B, b.nnz)
+    try:
+        layer.init_uniform(0, -0.05, 0.05)
+        layer.forward(keys, good, tids, B)
+        layer.backward_update(grad, "reduction")
+        assert layer.sync_status() == EMB_OK
+        layer.forward(keys, bad, tids, B)
+        assert layer.sync_status() == EMB_ERR_INVALID_ARG
+        layer.backward_update(grad, "reduction")
+        layer.sync_status()
+        layer.forward(keys, good, tids, B)
+        layer.backward_update(grad, "unique_hash")
+        assert layer.sync_status() == EMB_OK
     finally:
         layer.close()
 

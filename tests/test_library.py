@@ -32,6 +32,12 @@ def test_every_declared_symbol_is_exported(emb):
     assert sorted(emb.EXPORTS) == declared
 
 
+# page titles (and the one phrase for calls with no passage) a declaration's
+# comment may cite
+_PASSAGE_MARKS = ("HugeCTR slides", "NVIDIA EMBark", "Merlin overview article", "No passage: library convenience",
+                  "no counterpart on the pages", "Passage: as for")
+
+
 def test_every_declaration_is_documented():
     # each entry point sits in a group of declarations (with any #define or
     # enum it needs) directly under a comment: no blank line in between
@@ -47,6 +53,13 @@ def test_every_declaration_is_documented():
         while j >= 0 and lines[j].strip() and not lines[j].rstrip().endswith("*/"):
             j -= 1
         assert j >= 0 and lines[j].rstrip().endswith("*/"), m.group(1)
+        # the comment above the group names the passage the call follows, a
+        # page it points to through another call, or says it has none
+        k = j
+        while k >= 0 and "/*" not in lines[k]:
+            k -= 1
+        comment = " ".join(x.strip(" */") for x in lines[k:j + 1])
+        assert any(p in comment for p in _PASSAGE_MARKS), m.group(1)
     assert found == len(_declared_symbols())
 
 

@@ -55,6 +55,7 @@ def test_noalloc_unique_matches_emb_unique_on_two_calls_in_a_row():
     first = rng.integers(-(1 << 40), 1 << 40, size=UNIQUE_NOALLOC_MAX_KEYS, dtype=np.int64)
     first[::3] = first[7]                                  # heavy duplicates
     second = rng.integers(0, 50, size=777, dtype=np.int64)  # smaller, different range: stale contents must not leak
+    import oracle
     for keys in (first, second):
         ref = _call("emb_unique", keys, with_workspace=True)
         got = _call("emb_unique_noalloc", keys, with_workspace=False)
@@ -62,6 +63,11 @@ def test_noalloc_unique_matches_emb_unique_on_two_calls_in_a_row():
         assert got[0] == ref[0]
         for a, b in zip(got[1:], ref[1:]):
             assert np.array_equal(a, b)
+        # and the CPU oracle's sort + run-length unique, directly
+        u, inv, cnt, seg = oracle.unique(keys)
+        assert got[0] == u.size
+        assert np.array_equal(got[1], u) and np.array_equal(got[2], inv)
+        assert np.array_equal(got[3], cnt) and np.array_equal(got[4], seg)
 
 
 def test_noalloc_unique_rejects_sizes_beyond_its_scratch():

@@ -149,12 +149,29 @@ def _bits_for(v: int) -> int:
     return b
 
 
+def table_sort_bits(rows_max: int) -> int:
+    """Bits of the dedup sort's table-local keys: every row id of the largest
+    table plus an all-ones key for skipped lookups in a top digit of its own
+    (digits of at most 10 bits, passes balanced)."""
+    b = _bits_for(rows_max)
+    while True:
+        passes = -(-b // 10)
+        D = -(-b // passes)
+        top_shift = (passes - 1) * D
+        if ((rows_max - 1) >> top_shift) < (((1 << b) - 1) >> top_shift):
+            return b
+        b += 1
+
+
 def sort_passes(w: ci.Workload, variant: str) -> int:
-    """Radix-sort passes of the dedup (10-bit digits at most): the global id
-    of the reduction-based and the sort-based variants, which includes the
-    sentinel id one past the last row."""
-    total_rows = sum(s.rows for s in w.tables)
-    return -(-_bits_for(total_rows) // 10)
+    """Radix-sort passes over the lookups in the dedup: the reduction-based and
+    the sort-based variants sort each table's lookups on their table-local row
+    id; the hash-based one sorts them on the unique index (at most the lookups
+    or the rows, whichever is fewer)."""
+    if variant == "unique_hash":
+        total_rows = sum(s.rows for s in w.tables)
+        return -(-_bits_for(total_rows) // 10)
+    return -(-table_sort_bits(max(s.rows for s in w.tables)) // 10)
 
 
 def recorded_traffic(config: str, variant: str, phase: str, root: str = ROOT):

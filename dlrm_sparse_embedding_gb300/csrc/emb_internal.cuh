@@ -68,6 +68,45 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x)
     s = t;
 }
 
+// Packed fp32 pairs: one add.rn.f32x2 / sub.rn.f32x2 / mul.rn.f32x2 rounds
+// each half to nearest-even exactly as two scalar __fadd_rn / __fsub_rn /
+// __fmul_rn would, in one instruction.
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
+    return *reinterpret_cast<float2*>(&r);
+}
+
+__device__ __forceinline__ float2 sub2(float2 a, float2 b)
+{
+    unsigned long long r;
+    asm("sub.rn.f32x2 %0, %1, %2;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
+    return *reinterpret_cast<float2*>(&r);
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
+    return *reinterpret_cast<float2*>(&r);
+}
+
+// kahan_add on two columns at once.
+__device__ __forceinline__ void kahan_add2(float2& s, float2& c, float2 x)
+{
+    const float2 y = sub2(x, c);
+    const float2 t = add2(s, y);
+    c = sub2(sub2(t, s), y);
+    s = t;
+}
+
 __device__ __forceinline__ float4 load_w4(const void* w, int dtype, int64_t elem)
 {
     if (dtype == EMB_F32) return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(w) + elem));
@@ -169,38 +208,88 @@ __device__ __forceinline__ float group_sum(float v, int width, uint32_t mask)
 }
 
 // ---------------------------------------------------------------------------
-// radix sort of (key, u32 value) pairs
+// radix sort of (key, u32 value) pairs, optionally in independent segments
 // ---------------------------------------------------------------------------
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = 12;          // 3072-element tiles
+constexpr int kSortItems = 12;
+constexpr int kSortTile = kSortThreads * kSortItems;   // 3072-element tiles
+constexpr int kSortGroupTiles = 16;                     // tiles per group of the two-level count scan
 constexpr int kMaxDigitBits = 10;
 
 struct SortPlan {
     int64_t n_max;       // capacity in elements
+    int num_seg_max;     // segments the scratch is sized for
     int bits_max;        // keys < 2^bits_max
     int digit_bits;      // D
     int passes_max;      // ceil(bits_max / D)
     int64_t tiles_max;
-    size_t counts_bytes; // per-tile digit counts [2^D][tiles] u32
-    size_t totals_bytes; // digit totals [2^D] u32
+    int64_t groups_max;
+    size_t scratch_bytes;   // descriptors, per-tile counts and per-group sums of one sort
 };
 
-SortPlan make_sort_plan(int64_t n_max, int bits_max);
+SortPlan make_sort_plan(int64_t n_max, int bits_max, int num_seg_max = 1);
 
-// Sorts (keys_in, vals_in) ascending by key, stable, into (keys_out,
-// vals_out), using (keys_tmp, vals_tmp) as ping-pong space.  n is
-// n_dev ? *n_dev : n_host (n_host bounds the grid).  Only the low
-// bits_dev ? *bits_dev : plan.bits_max bits are sorted; at least one pass
-// always runs.  vals_in == nullptr means value = index.  key_sub (nullable,
-// 64-bit keys only) is subtracted from every input key first.  `counts`
-// (plan.counts_bytes) and `totals` (plan.totals_bytes) are scratch that need
-// no initial contents.  Returns the number of kernels launched, or -1 on a
-// launch error.
+// Bits of the layer sort's table-local keys for tables of at most rows_max
+// rows: enough for every row id and for the all-ones key of a skipped lookup
+// in a top digit of its own.
+int table_sort_bits(int64_t rows_max);
+
+// One sort.  Keys and values move from (keys_in, vals_in) to (keys_out,
+// vals_out) through (keys_tmp, vals_tmp), stable, ascending by key.
+// n = n_dev ? min(*n_dev, n_host) : n_host; only the low
+// (bits_dev ? *bits_dev : plan bits) bits are sorted.  vals_in == nullptr
+// means value = index.  key_sub (nullable, plain sorts) is subtracted from
+// every key first.
+// Segments: with offsets == nullptr the input is one segment.  Otherwise
+// segment s ends at clamp(offsets[(s+1)*stride]) (made non-decreasing, the
+// last one at n) and each segment is sorted in place.  With `tables` set (the
+// layer sort, u32 keys, one segment per table) keys are global row ids: each
+// is ranked by its id local to the segment's table, ids at or above
+// `sentinel` (or outside the table) rank last and come out as `sentinel`
+// behind every valid id of every segment, so the output is the ascending sort
+// of the ids.
+struct SortArgs {
+    const void* keys_in;
+    const uint32_t* vals_in;
+    void* keys_out;
+    uint32_t* vals_out;
+    void* keys_tmp;
+    uint32_t* vals_tmp;
+    int64_t n_host;
+    const int64_t* n_dev;
+    const int32_t* bits_dev;
+    const uint64_t* key_sub;
+    const int64_t* offsets;
+    int32_t stride;
+    int32_t num_seg;
+    const TableDev* tables;
+    uint32_t sentinel;
+    // filled in by radix_sort_pairs from the plan
+    int bits_max;
+    int D;
+    uint64_t skip_key;
+};
+
+inline SortArgs sort_args(const void* keys_in, const uint32_t* vals_in, void* keys_out, uint32_t* vals_out,
+                          void* keys_tmp, uint32_t* vals_tmp, int64_t n_host)
+{
+    SortArgs a{};
+    a.keys_in = keys_in;
+    a.vals_in = vals_in;
+    a.keys_out = keys_out;
+    a.vals_out = vals_out;
+    a.keys_tmp = keys_tmp;
+    a.vals_tmp = vals_tmp;
+    a.n_host = n_host;
+    a.stride = 1;
+    a.num_seg = 1;
+    return a;
+}
+
+// Launches the sort; `scratch` holds plan.scratch_bytes and needs no initial
+// contents.  Returns the number of kernels launched, or -1 on a launch error.
 template <typename K>
-int radix_sort_pairs(const SortPlan& plan, const K* keys_in, const uint32_t* vals_in,
-                     K* keys_out, uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp,
-                     uint32_t* counts, uint32_t* totals, int64_t n_host, const int64_t* n_dev,
-                     const int32_t* bits_dev, const uint64_t* key_sub, cudaStream_t st);
+int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // run-length encoding of sorted keys (unique / counts / segment offsets)
@@ -262,6 +351,7 @@ struct FwdArgs {
     const TableDev* tables;
     uint32_t* gid_out;          // global row id per lookup (sentinel when skipped)
     uint32_t* bag_out;          // bag id per lookup
+    int64_t* tab_start;         // [T] first lookup of each table (written with the ids)
     float* bag_scale;           // 1/L per mean-pooled bag
     uint32_t sentinel;          // = total rows: sorts after every valid id
     int64_t warps_per_table;

@@ -9,13 +9,18 @@
 // Layout: bag j = t*B + b.  A warp owns 32 consecutive bags of one table,
 // split among groups of Lr = next_pow2(dim/4) lanes; each lane covers 4
 // columns (one 16-byte fp32 or 8-byte 16-bit load per row), and a group owns
-// Lr consecutive bags.  Because those bags are adjacent in the CSR, their
-// keys form one contiguous range, which the group streams through: keys are
-// loaded one per lane and broadcast inside the group, eight rows per lane are
-// kept in flight, and each bag's compensated fp32 sum is stored into its slice
-// of the concatenated output as soon as the stream passes the bag's end.  The same pass writes, for the
-// backward, the global row id (row_base + key) and the bag of every lookup,
-// and 1/L of every mean-pooled bag.
+// Lr consecutive bags.  A group whose bags all hold one key copies each row
+// straight to its output slice.  Otherwise the group pools its bags one after
+// another: a bag's keys are loaded in windows of up to 32 (spread over the
+// group's lanes), eight rows per lane are kept in flight, and every row is a
+// term of the bag's cascaded compensated fp32 sum (two columns per packed
+// instruction), so the pooled value is as accurate as a sum in twice the
+// working precision rounded once; the result is stored into the bag's slice
+// of the concatenated output.  The same
+// pass writes, for the backward, the global row id (row_base + key) and the
+// bag of every lookup, and 1/L of every mean-pooled bag.
+#include <type_traits>
+
 #include "emb_internal.cuh"
 
 namespace emb {
@@ -24,14 +29,6 @@ namespace emb {
 namespace {
 
 constexpr int kThreads = 256;
-
-__device__ __forceinline__ void kahan_add(float& s, float& c, float x)
-{
-    float y = __fsub_rn(x, c);
-    float t = __fadd_rn(s, y);
-    c = __fsub_rn(__fsub_rn(t, s), y);
-    s = t;
-}
 
 __device__ __forceinline__ float4 load_row4(const void* w, int dtype, int64_t elem)
 {
@@ -57,49 +54,7 @@ __device__ __forceinline__ void prefetch_row_l2(const TableDev& tb, int64_t key)
     for (int off = 0; off < tb.dim * wb; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
 }
 
-// Running state of a group streaming through its bags' keys.
-struct BagStream {
-    float4 s, c;        // compensated sum of the current bag (4 columns per lane)
-    int cur;            // current bag, index within the group
-    int64_t cur_end;    // its end offset
-};
-
-__device__ __forceinline__ void kahan_add4(BagStream& st, float4 x)
-{
-    kahan_add(st.s.x, st.c.x, x.x);
-    kahan_add(st.s.y, st.c.y, x.y);
-    kahan_add(st.s.z, st.c.z, x.z);
-    kahan_add(st.s.w, st.c.w, x.w);
-}
-
-__device__ __forceinline__ float4 add4(float4 a, float4 b)
-{
-    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
-}
-
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;
-
-// Closes (scales and stores) every bag that ends at position `pos`, empty bags included.
-__device__ __forceinline__ void close_bags(BagStream& st, int64_t pos, int nbg, uint32_t gmask, int Lr, int my_len,
-                                           int64_t my_end, bool mean, bool colok, float* out_col, int64_t bg0,
-                                           int64_t ld)
-{
-    while (st.cur < nbg && st.cur_end == pos) {
-        const int L = __shfl_sync(gmask, my_len, st.cur, Lr);
-        float4 r = make_float4(__fsub_rn(st.s.x, st.c.x), __fsub_rn(st.s.y, st.c.y), __fsub_rn(st.s.z, st.c.z),
-                               __fsub_rn(st.s.w, st.c.w));
-        if (mean && L > 0) {
-            const float fl = (float)L;
-            r = make_float4(__fdiv_rn(r.x, fl), __fdiv_rn(r.y, fl), __fdiv_rn(r.z, fl), __fdiv_rn(r.w, fl));
-        }
-        if (colok) __stcs(reinterpret_cast<float4*>(out_col + (bg0 + st.cur) * ld), r);
-        st.s = make_float4(0.f, 0.f, 0.f, 0.f);
-        st.c = st.s;
-        ++st.cur;
-        const int64_t e = __shfl_sync(gmask, my_end, st.cur < nbg ? st.cur : 0, Lr);
-        st.cur_end = st.cur < nbg ? e : INT64_MAX;
-    }
-}
 
 // The row of a lookup code in the inference forward: a table row, or (high
 // bit set, tables with a cache) a row of the table's fp16 cache.
@@ -130,6 +85,173 @@ __device__ __forceinline__ int64_t cache_slot_of(const TableDev& tb, int64_t row
     return -1;
 }
 
+// One term of a cascaded compensated sum on two columns at once (Ogita,
+// Rump & Oishi 2005, "Accurate sum and dot product", algorithm Sum2): TwoSum
+// (Knuth) splits s + x into the rounded sum and its exact rounding error, and
+// the errors are added up separately.  The result s + c is as accurate as
+// summing in twice the working precision and rounding once, whatever the
+// cancellation.
+__device__ __forceinline__ void sum2_add(float2& s, float2& c, float2 x)
+{
+    const float2 t = add2(s, x);
+    const float2 z = sub2(t, s);
+    const float2 e = add2(sub2(s, sub2(t, z)), sub2(x, z));
+    c = add2(c, e);
+    s = t;
+}
+
+// A lookup's 4 columns of this lane as they travel from memory to the sum:
+// fp32 rows as float4, 16-bit rows as their raw 8 bytes (converted when the
+// row is added), and in the inference forward always as float4 (a cached row
+// comes from the table's fp16 cache).
+template <int DT, bool kInfer>
+struct RowBits {
+    using T = typename std::conditional<DT == EMB_F32 || kInfer, float4, uint2>::type;
+};
+
+__device__ __forceinline__ float4 bits16_to_f32(uint2 r, int dtype)
+{
+    if (dtype == EMB_F16) {
+        const float2 fa = __half22float2(*reinterpret_cast<__half2*>(&r.x));
+        const float2 fb = __half22float2(*reinterpret_cast<__half2*>(&r.y));
+        return make_float4(fa.x, fa.y, fb.x, fb.y);
+    }
+    const float2 fa = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r.x));
+    const float2 fb = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r.y));
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+
+template <int DT, bool kInfer>
+__device__ __forceinline__ typename RowBits<DT, kInfer>::T fetch_row(const TableDev& tb, const char* wlane, uint32_t kq,
+                                                                      uint32_t rbytes, int li)
+{
+    const char* p = wlane + (uint64_t)kq * rbytes;
+    if constexpr (kInfer) {
+        if (tb.cache_w && (kq & kCacheBit)) return load_cached_row4(tb, kq & ~kCacheBit, li);
+        if constexpr (DT == EMB_F32) return __ldg(reinterpret_cast<const float4*>(p));
+        else return bits16_to_f32(__ldg(reinterpret_cast<const uint2*>(p)), DT);
+    } else {
+        if constexpr (DT == EMB_F32) return __ldg(reinterpret_cast<const float4*>(p));
+        else return __ldg(reinterpret_cast<const uint2*>(p));
+    }
+}
+
+template <int DT, bool kInfer>
+__device__ __forceinline__ float4 row_f32(typename RowBits<DT, kInfer>::T r)
+{
+    if constexpr (DT == EMB_F32 || kInfer) return r;
+    else return bits16_to_f32(r, DT);
+}
+
+template <int DT, bool kInfer>
+__device__ __forceinline__ typename RowBits<DT, kInfer>::T zero_row()
+{
+    if constexpr (DT == EMB_F32 || kInfer) return make_float4(0.f, 0.f, 0.f, 0.f);
+    else return make_uint2(0u, 0u);
+}
+
+// Pools the group's bags one after another (bags of several keys) of a table
+// stored as DT.  Positions fit in 32 bits (fewer than 2^31 lookups).  A bag's
+// keys are taken in windows of WIN (32; 8 or 16 for rows of at most 8
+// columns): lane li loads positions w + li + j*LR (j < KPL), checks them,
+// writes their global ids and bag for the backward, and keeps a 32-bit row
+// code per key (kNoRow for a skipped lookup).  The window's rows are then
+// requested eight per lane at a time (each key's code broadcast from the lane
+// that loaded it) and added in key order as terms of the bag's cascaded
+// compensated sum, two columns per instruction; a skipped key or a position
+// past the bag adds an exact zero, which leaves the sum unchanged.  The
+// result is scaled for mean pooling and stored into the bag's output slice.
+template <int LR, bool kInfer, int DT>
+__device__ __forceinline__ void pool_bags(const FwdArgs& a, const TableDev& tb, const int64_t* kp, int li,
+                                          uint32_t gmask, int64_t j0, int nbg, int my_start, int my_end,
+                                          bool my_tid_ok, bool colok, float* out_col, int64_t bg0)
+{
+    constexpr int KPL = LR >= 4 ? 32 / LR : 8;   // keys each lane loads per window
+    constexpr int WIN = KPL * LR;                // keys per window
+    using Row = typename RowBits<DT, kInfer>::T;
+    const char* wlane = static_cast<const char*>(tb.w) + (DT == EMB_F32 ? 16 : 8) * li;
+    const uint32_t rbytes = (uint32_t)tb.dim * (DT == EMB_F32 ? 4u : 2u);
+    const bool mean = tb.pooling == EMB_POOL_MEAN;
+    for (int k = 0; k < nbg; ++k) {
+        const int s0 = __shfl_sync(gmask, my_start, k, LR);
+        const int e0 = __shfl_sync(gmask, my_end, k, LR);
+        const bool tok = __shfl_sync(gmask, my_tid_ok, k, LR);
+        float2 sa = make_float2(0.f, 0.f), sb = sa, ca = sa, cb = sa;
+        for (int w = s0; w < e0; w += WIN) {
+            uint32_t kk[KPL];
+#pragma unroll
+            for (int j = 0; j < KPL; ++j) {
+                const int p = w + li + j * LR;
+                kk[j] = kNoRow;
+                if (p < e0) {
+                    const int64_t key = __ldg(kp + p);
+                    const bool valid = tok && key >= 0 && key < tb.rows;
+                    if (!kInfer && a.write_ids) {
+                        a.gid_out[p] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
+                        a.bag_out[p] = (uint32_t)(j0 + k);
+                    }
+                    if (!valid && tok && !(kInfer && tb.dynamic)) atomicOr(a.err, ERRBIT_KEY_RANGE);
+                    if (valid) {
+                        kk[j] = (uint32_t)key;
+                        // a cached row travels as its cache slot with kCacheBit set
+                        // (tables with a cache have fewer than 2^31 rows)
+                        if (kInfer && tb.cache_map) {
+                            const int64_t cs = cache_slot_of(tb, key);
+                            if (cs >= 0) kk[j] = kCacheBit | (uint32_t)cs;
+                        }
+                    }
+                }
+            }
+            const int n = e0 - w < WIN ? e0 - w : WIN;
+#pragma unroll
+            for (int b = 0; b < WIN; b += kPrefetch) {
+                if (b >= n) break;
+                Row v[kPrefetch];
+#pragma unroll
+                for (int u = 0; u < kPrefetch; ++u) {
+                    const int q = b + u;
+                    const uint32_t kq = __shfl_sync(gmask, kk[q / LR], q % LR, LR);
+                    v[u] = zero_row<DT, kInfer>();
+                    if (q < n && kq != kNoRow && colok) v[u] = fetch_row<DT, kInfer>(tb, wlane, kq, rbytes, li);
+                }
+#pragma unroll
+                for (int u = 0; u < kPrefetch; ++u) {
+                    const float4 x = row_f32<DT, kInfer>(v[u]);
+                    sum2_add(sa, ca, make_float2(x.x, x.y));
+                    sum2_add(sb, cb, make_float2(x.z, x.w));
+                }
+            }
+        }
+        const float2 ra = add2(sa, ca), rb = add2(sb, cb);
+        float4 r = make_float4(ra.x, ra.y, rb.x, rb.y);
+        const int L = e0 - s0;
+        if (mean && L > 0) {
+            const float fl = (float)L;
+            r = make_float4(__fdiv_rn(r.x, fl), __fdiv_rn(r.y, fl), __fdiv_rn(r.z, fl), __fdiv_rn(r.w, fl));
+        }
+        if (colok) __stcs(reinterpret_cast<float4*>(out_col + (bg0 + k) * a.ld), r);
+    }
+}
+
+// The pooling of multi-key bags for a table of row width Lr lanes and
+// storage type dt.
+template <bool kInfer, int DT>
+__device__ __forceinline__ void pool_bags_lr(int Lr, const FwdArgs& a, const TableDev& tb, const int64_t* kp, int li,
+                                             uint32_t gmask, int64_t j0, int nbg, int my_start, int my_end,
+                                             bool my_tid_ok, bool colok, float* out_col, int64_t bg0)
+{
+#define POOL(LR) pool_bags<LR, kInfer, DT>(a, tb, kp, li, gmask, j0, nbg, my_start, my_end, my_tid_ok, colok, out_col, bg0)
+    switch (Lr) {
+        case 1: POOL(1); break;
+        case 2: POOL(2); break;
+        case 4: POOL(4); break;
+        case 8: POOL(8); break;
+        case 16: POOL(16); break;
+        default: POOL(32); break;
+    }
+#undef POOL
+}
+
 // kMinBlocks: resident blocks per SM the register budget is sized for.  With
 // 16-bit rows a lane holds half the row data in flight, and 4 blocks (64
 // registers) measure faster; fp32 rows take 3 (80 registers).
@@ -137,6 +259,8 @@ __device__ __forceinline__ int64_t cache_slot_of(const TableDev& tb, int64_t row
 // from the fp16 cache (the lane that loads the key probes the cache map), a
 // dynamic table's id it never saw is skipped silently, and nothing is written
 // for a backward (no ids, no bag scales).
+constexpr int kBlocks16 = 4;   // resident blocks of the kernel for layers of 16-bit tables only
+
 template <int kMinBlocks, bool kInfer>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
 {
@@ -153,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
     const uint32_t gmask = Lr == 32 ? 0xffffffffu : (((1u << Lr) - 1u) << (g * Lr));
     const bool colok = 4 * li < tb.dim;
     const bool mean = tb.pooling == EMB_POOL_MEAN;
-    const uint32_t lowmask = Lr == 32 ? 0xffffffffu : ((1u << Lr) - 1u);
 
     // this group owns bags bg0 .. bg0+nbg-1 of table t; lane li describes bag li
     const int64_t bg0 = (gw - (int64_t)t * a.warps_per_table) * 32 + (int64_t)g * Lr;
@@ -181,6 +304,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
         }
     }
     if (__any_sync(gmask, my_bad || K0 != K0raw) && li == 0) atomicOr(a.err, ERRBIT_OFFSETS);
+    // the first group of a table records where the table's lookups start (the
+    // backward's sort takes each table's lookups as one segment)
+    if (!kInfer && a.write_ids && bg0 == 0 && li == 0) a.tab_start[t] = K0;
     int64_t my_start = __shfl_up_sync(gmask, my_end, 1, Lr);
     if (li == 0) my_start = K0;
     if (li < nbg) {
@@ -229,87 +355,18 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
         return;
     }
 
-    BagStream st;
-    st.s = make_float4(0.f, 0.f, 0.f, 0.f);
-    st.c = st.s;
-    st.cur = 0;
-    st.cur_end = __shfl_sync(gmask, my_end, 0, Lr);
-#define CLOSE_BAGS(pos) close_bags(st, (pos), nbg, gmask, Lr, my_len, my_end, mean, colok, out_col, bg0, a.ld)
-
-    CLOSE_BAGS(K0);
-    for (int64_t base = K0; base < K1; base += Lr) {
-        const int64_t i = base + li;
-        const bool in = i < K1;
-        const int64_t key = in ? __ldg(kp + i) : 0;
-        // bag of position i = number of the group's bags that end at or before i
-        int k = 0;
-        for (int stp = Lr >> 1; stp > 0; stp >>= 1) {
-            const int64_t e = __shfl_sync(gmask, my_end, k + stp - 1, Lr);
-            if (e <= i) k += stp;
-        }
-        const bool tok = __shfl_sync(gmask, my_tid_ok, k, Lr);
-        const int64_t kend = __shfl_sync(gmask, my_end, k, Lr);
-        const bool valid = in && tok && key >= 0 && key < tb.rows;
-        if (in) {
-            if (!kInfer && a.write_ids) {
-                a.gid_out[i] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
-                a.bag_out[i] = (uint32_t)(j0 + k);
-            }
-            if (!valid && tok && !(kInfer && tb.dynamic)) atomicOr(a.err, ERRBIT_KEY_RANGE);
-        }
-        // bit u: a bag ends right after position base + u
-        const uint32_t endbits = (__ballot_sync(gmask, in && kend == i + 1) >> (g * Lr)) & lowmask;
-        // rows < 2^32 per table, so a key travels as 32 bits; kNoRow = skipped.
-        // A cache slot (tables with a cache have fewer than 2^31 rows) travels
-        // with kCacheBit set.
-        uint32_t kk = valid ? (uint32_t)key : kNoRow;
-        if (kInfer && valid && tb.cache_map) {
-            const int64_t cs = cache_slot_of(tb, key);
-            if (cs >= 0) kk = kCacheBit | (uint32_t)cs;
-        }
-        const int cnt = (int)((K1 - base) < Lr ? (K1 - base) : Lr);
-        for (int q = 0; q < cnt; q += kPrefetch) {
-            float4 v[kPrefetch];
-#pragma unroll
-            for (int u = 0; u < kPrefetch; ++u) {
-                const uint32_t kq = __shfl_sync(gmask, kk, (q + u) & (Lr - 1), Lr);
-                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (kq != kNoRow && q + u < cnt && colok)
-                    v[u] = (kInfer && tb.cache_w && (kq & kCacheBit))
-                               ? load_cached_row4(tb, kq & ~kCacheBit, li)
-                               : load_row4(tb.w, tb.dtype, (int64_t)kq * tb.dim + 4 * li);
-            }
-            // Four rows of one bag are added as a tree ((v0+v1)+(v2+v3)) and
-            // compensated into the bag's sum in one step.  Where a bag ends
-            // inside the four, rows are added in pairs instead, and a bag
-            // ending inside a pair takes the first row alone.
-#pragma unroll
-            for (int h = 0; h < kPrefetch; h += 4) {
-                if (q + h >= cnt) continue;
-                const uint32_t eb = endbits >> (q + h);
-                if (q + h + 4 <= cnt && (eb & 7u) == 0) {
-                    kahan_add4(st, add4(add4(v[h], v[h + 1]), add4(v[h + 2], v[h + 3])));
-                    if (eb & 8u) CLOSE_BAGS(base + q + h + 4);
-                    continue;
-                }
-#pragma unroll
-                for (int u = h; u < h + 4; u += 2) {
-                    if (q + u < cnt) {
-                        const bool split = (endbits >> (q + u)) & 1u;
-                        const float4 w1 = split ? make_float4(0.f, 0.f, 0.f, 0.f) : v[u + 1];
-                        kahan_add4(st, add4(v[u], w1));
-                        if (split) {
-                            CLOSE_BAGS(base + q + u + 1);
-                            if (q + u + 1 < cnt) kahan_add4(st, v[u + 1]);
-                        }
-                        if ((endbits >> (q + u + 1)) & 1u) CLOSE_BAGS(base + q + u + 2);
-                    }
-                }
-            }
-        }
-    }
-    CLOSE_BAGS(K1);
-#undef CLOSE_BAGS
+    // several keys per bag: the group pools its bags one after another
+    // positions fit in 32 bits (lanes past the group's bags are never read)
+    // the kernel for layers whose tables all store 16-bit rows has no fp32 path
+    if (kMinBlocks != kBlocks16 && tb.dtype == EMB_F32)
+        pool_bags_lr<kInfer, EMB_F32>(Lr, a, tb, kp, li, gmask, j0, nbg, (int)my_start, (int)my_end, my_tid_ok, colok,
+                                      out_col, bg0);
+    else if (tb.dtype == EMB_F16)
+        pool_bags_lr<kInfer, EMB_F16>(Lr, a, tb, kp, li, gmask, j0, nbg, (int)my_start, (int)my_end, my_tid_ok, colok,
+                                      out_col, bg0);
+    else
+        pool_bags_lr<kInfer, EMB_BF16>(Lr, a, tb, kp, li, gmask, j0, nbg, (int)my_start, (int)my_end, my_tid_ok,
+                                       colok, out_col, bg0);
 }
 
 // Global row id and bag of every lookup, nothing else: the forward's id
@@ -341,6 +398,7 @@ __global__ void __launch_bounds__(kThreads) fwd_ids(FwdArgs a)
         if (lane >= off && lane < nbg && v > my_end) my_end = v;
     }
     const int64_t K1 = __shfl_sync(0xffffffffu, my_end, nbg - 1);
+    if (bg0 == 0 && lane == 0) a.tab_start[t] = K0;
     for (int64_t base = K0; base < K1; base += 32) {
         const int64_t i = base + lane;
         int k = 0;
@@ -377,12 +435,12 @@ int launch_forward(const FwdArgs& a, cudaStream_t st)
     const unsigned blocks = (unsigned)((warps * 32 + kThreads - 1) / kThreads);
     if (a.infer) {
         if (a.rows16)
-            fwd_pool<4, true><<<blocks, kThreads, 0, st>>>(a);
+            fwd_pool<kBlocks16, true><<<blocks, kThreads, 0, st>>>(a);
         else
             fwd_pool<3, true><<<blocks, kThreads, 0, st>>>(a);
     } else {
         if (a.rows16)
-            fwd_pool<4, false><<<blocks, kThreads, 0, st>>>(a);
+            fwd_pool<kBlocks16, false><<<blocks, kThreads, 0, st>>>(a);
         else
             fwd_pool<3, false><<<blocks, kThreads, 0, st>>>(a);
     }

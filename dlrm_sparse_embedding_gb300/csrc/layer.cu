@@ -30,8 +30,8 @@ struct emb_layer {
     float* bag_scale = nullptr;
     // sort buffers
     uint32_t *sk = nullptr, *sv = nullptr, *tk = nullptr, *tv = nullptr;
-    uint32_t* sort_counts = nullptr;   // per-tile digit counts
-    uint32_t* sort_totals = nullptr;   // digit totals
+    void* sort_scratch = nullptr;      // descriptors and counts of one sort (the largest plan's)
+    int64_t* tab_start = nullptr;      // [T+1] first lookup of each table in the last forward
     SortPlan plan_gid{}, plan_inv{}, plan_ukey{};
     // dedup results
     int64_t* num_unique = nullptr;
@@ -248,8 +248,7 @@ unsigned grid_for(int64_t n, int threads, int64_t cap = 16384)
 struct UniqueWs {
     uint64_t *k_tmp, *k_out;
     uint32_t *v_tmp, *v_out;
-    uint32_t* counts;
-    uint32_t* totals;
+    void* sort_scratch;
     int32_t* seg;
     void* rle;
     unsigned long long* mm;
@@ -273,8 +272,7 @@ UniqueWs unique_ws_layout(int64_t n, char* base)
     w.k_out = reinterpret_cast<uint64_t*>(take(sizeof(uint64_t) * m));
     w.v_tmp = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t) * m));
     w.v_out = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t) * m));
-    w.counts = reinterpret_cast<uint32_t*>(take(plan.counts_bytes));
-    w.totals = reinterpret_cast<uint32_t*>(take(plan.totals_bytes));
+    w.sort_scratch = take(plan.scratch_bytes);
     w.seg = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (m + 1)));
     w.rle = take(rle_scratch_bytes(m));
     w.mm = reinterpret_cast<unsigned long long*>(take(2 * sizeof(unsigned long long)));
@@ -422,14 +420,15 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
     const int64_t n = max_nnz;
     L->max_unique = n < (int64_t)total_rows ? n : (int64_t)total_rows;
     const int gid_bits = bits_for(total_rows);                 // ids 0..total_rows (sentinel)
-    L->plan_gid = make_sort_plan(n, gid_bits);
+    int64_t rows_max = 1;
+    for (int t = 0; t < num_tables; ++t) rows_max = specs[t].rows > rows_max ? specs[t].rows : rows_max;
+    // the lookups' ids are sorted table by table on their table-local row
+    L->plan_gid = make_sort_plan(n, table_sort_bits(rows_max), num_tables);
     L->plan_ukey = make_sort_plan(L->max_unique, gid_bits);
     L->plan_inv = make_sort_plan(n, bits_for((uint64_t)L->max_unique));
-    size_t counts_bytes = L->plan_gid.counts_bytes, totals_bytes = L->plan_gid.totals_bytes;
-    for (const SortPlan* pl : {&L->plan_inv, &L->plan_ukey}) {
-        if (pl->counts_bytes > counts_bytes) counts_bytes = pl->counts_bytes;
-        if (pl->totals_bytes > totals_bytes) totals_bytes = pl->totals_bytes;
-    }
+    size_t sort_scratch_bytes = L->plan_gid.scratch_bytes;
+    for (const SortPlan* pl : {&L->plan_inv, &L->plan_ukey})
+        if (pl->scratch_bytes > sort_scratch_bytes) sort_scratch_bytes = pl->scratch_bytes;
     uint64_t cap = 1024;
     while (cap < 2 * (uint64_t)(L->max_unique > 0 ? L->max_unique : 1)) cap <<= 1;
     L->hmask = (uint32_t)(cap - 1);
@@ -438,8 +437,8 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
     ok = ok && dalloc_n(L, &L->d_tables, num_tables) && dalloc_n(L, &L->gid, n) && dalloc_n(L, &L->bag, n) &&
          dalloc_n(L, &L->bag_scale, (int64_t)num_tables * max_batch) && dalloc_n(L, &L->sk, n) &&
          dalloc_n(L, &L->sv, n) && dalloc_n(L, &L->tk, n) && dalloc_n(L, &L->tv, n) &&
-         dalloc(L, reinterpret_cast<void**>(&L->sort_counts), counts_bytes) &&
-         dalloc(L, reinterpret_cast<void**>(&L->sort_totals), totals_bytes) && dalloc_n(L, &L->num_unique, 1) &&
+         dalloc(L, &L->sort_scratch, sort_scratch_bytes) && dalloc_n(L, &L->tab_start, num_tables + 1) &&
+         dalloc_n(L, &L->num_unique, 1) &&
          dalloc_n(L, &L->seg_off, n + 1) && dalloc_n(L, &L->cnt, n) && dalloc_n(L, &L->inverse, n) &&
          dalloc_n(L, &L->uniq32, n) && dalloc(L, &L->rle_scratch, rle_scratch_bytes(n)) &&
          dalloc_n(L, &L->htable, (int64_t)cap) && dalloc_n(L, &L->slot_rank, (int64_t)cap) &&
@@ -536,9 +535,14 @@ static int launch_dedup(emb_layer* L, int32_t variant, int64_t n, cudaStream_t s
     r.key_limit = limit;
     r.key_limit_dev = nullptr;
     r.gid_of_key = nullptr;
+    // the lookups' ids, table by table (the forward wrote each table's first lookup)
+    SortArgs by_table = sort_args(L->gid, L->bag, L->sk, L->sv, L->tk, L->tv, n);
+    by_table.offsets = L->tab_start;
+    by_table.num_seg = L->T;
+    by_table.tables = L->d_tables;
+    by_table.sentinel = limit;
     if (variant == EMB_BWD_REDUCTION) {
-        rc = track(L, radix_sort_pairs<uint32_t>(L->plan_gid, L->gid, L->bag, L->sk, L->sv, L->tk, L->tv,
-                                                 L->sort_counts, L->sort_totals, n, nullptr, nullptr, nullptr, st));
+        rc = track(L, radix_sort_pairs<uint32_t>(L->plan_gid, by_table, L->sort_scratch, st));
         if (rc == EMB_OK && L->keep_dedup)
             rc = track(L, rle_sorted<uint32_t>(L->sk, nullptr, n, limit - 1u, nullptr, nullptr, L->uniq32, L->seg_off,
                                                L->cnt, nullptr, L->num_unique, L->rle_scratch, nullptr, st));
@@ -547,8 +551,8 @@ static int launch_dedup(emb_layer* L, int32_t variant, int64_t n, cudaStream_t s
         L->last_unique32 = L->uniq32;
         L->last_sorted_bags = L->sv;
     } else if (variant == EMB_BWD_UNIQUE_SORT) {
-        rc = track(L, radix_sort_pairs<uint32_t>(L->plan_gid, L->gid, nullptr, L->sk, L->sv, L->tk, L->tv,
-                                                 L->sort_counts, L->sort_totals, n, nullptr, nullptr, nullptr, st));
+        by_table.vals_in = nullptr;   // values: positions, for the inverse
+        rc = track(L, radix_sort_pairs<uint32_t>(L->plan_gid, by_table, L->sort_scratch, st));
         if (rc == EMB_OK)
             rc = track(L, rle_sorted<uint32_t>(L->sk, L->sv, n, limit - 1u, nullptr, nullptr, L->uniq32, L->seg_off,
                                                L->cnt, reinterpret_cast<int32_t*>(L->inverse), L->num_unique,
@@ -563,17 +567,19 @@ static int launch_dedup(emb_layer* L, int32_t variant, int64_t n, cudaStream_t s
         rc = track(L, launch_hash_insert(L->gid, n, limit, L->htable, L->hmask, slot_of, L->ukey, L->uslot,
                                          L->num_unique, L->err, st));
         const int64_t umax = n < L->max_unique ? n : L->max_unique;
-        if (rc == EMB_OK)
-            rc = track(L, radix_sort_pairs<uint32_t>(L->plan_ukey, L->ukey, L->uslot, L->ukey_s, L->uslot_s, L->tk,
-                                                     L->tv, L->sort_counts, L->sort_totals, umax, L->num_unique, nullptr,
-                                                     nullptr, st));
+        if (rc == EMB_OK) {
+            SortArgs sa = sort_args(L->ukey, L->uslot, L->ukey_s, L->uslot_s, L->tk, L->tv, umax);
+            sa.n_dev = L->num_unique;
+            rc = track(L, radix_sort_pairs<uint32_t>(L->plan_ukey, sa, L->sort_scratch, st));
+        }
         if (rc == EMB_OK)
             rc = track(L, launch_hash_rank_inverse(L->uslot_s, L->num_unique, L->slot_rank, L->bits_dev, L->seg_off,
                                                    slot_of, n, L->inverse, st));
-        if (rc == EMB_OK)
-            rc = track(L, radix_sort_pairs<uint32_t>(L->plan_inv, L->inverse, L->bag, L->sk, L->sv, L->tk, L->tv,
-                                                     L->sort_counts, L->sort_totals, n, nullptr, L->bits_dev, nullptr,
-                                                     st));
+        if (rc == EMB_OK) {
+            SortArgs sa = sort_args(L->inverse, L->bag, L->sk, L->sv, L->tk, L->tv, n);
+            sa.bits_dev = L->bits_dev;
+            rc = track(L, radix_sort_pairs<uint32_t>(L->plan_inv, sa, L->sort_scratch, st));
+        }
         if (rc == EMB_OK) rc = track(L, launch_seg_from_sorted(L->sk, n, L->num_unique, L->seg_off, L->cnt, st));
         r.skeys = L->sk;
         r.sbags = L->sv;
@@ -605,6 +611,7 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
     a.tables = L->d_tables;
     a.gid_out = L->gid;
     a.bag_out = L->bag;
+    a.tab_start = L->tab_start;
     a.bag_scale = L->bag_scale;
     a.sentinel = (uint32_t)L->total_rows;
     a.warps_per_table = (batch + 31) / 32;
@@ -817,9 +824,10 @@ int emb_unique(const int64_t* keys, int64_t n, int64_t* unique, int32_t* inverse
     }
     SortPlan plan = make_sort_plan(n, 64);
     if (launch_minmax(keys, n, w.mm, w.key_sub, w.bits, st) < 0) return EMB_ERR_CUDA;
-    if (radix_sort_pairs<uint64_t>(plan, reinterpret_cast<const uint64_t*>(keys), nullptr, w.k_out, w.v_out, w.k_tmp,
-                                   w.v_tmp, w.counts, w.totals, n, nullptr, w.bits, w.key_sub, st) < 0)
-        return EMB_ERR_CUDA;
+    SortArgs sa = sort_args(keys, nullptr, w.k_out, w.v_out, w.k_tmp, w.v_tmp, n);
+    sa.bits_dev = w.bits;
+    sa.key_sub = w.key_sub;
+    if (radix_sort_pairs<uint64_t>(plan, sa, w.sort_scratch, st) < 0) return EMB_ERR_CUDA;
     if (rle_sorted<uint64_t>(w.k_out, w.v_out, n, ~0ull, w.key_sub, unique, nullptr, seg, counts, inverse, num_unique,
                              w.rle, nullptr, st) < 0)
         return EMB_ERR_CUDA;
@@ -937,6 +945,7 @@ int emb_forward_infer(emb_layer* L, const int64_t* keys, const int64_t* offsets,
     a.tables = L->d_tables;
     a.gid_out = nullptr;
     a.bag_out = nullptr;
+    a.tab_start = nullptr;
     a.bag_scale = nullptr;
     a.sentinel = (uint32_t)L->total_rows;
     a.warps_per_table = (batch + 31) / 32;

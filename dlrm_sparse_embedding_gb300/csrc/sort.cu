@@ -4,16 +4,25 @@
 // de recomendacion a escala", section "Integracion del cluster": RB reduces
 // over equal keys, UB dedups the keys first).
 //
-// Each pass runs three kernels over 3072-key tiles: a per-tile digit
-// histogram, a scan of each digit's row over tiles, and stable in-tile
-// ranking in shared memory with coalesced runs written to bucket start + tile
-// offset.  No tile waits on another.  (A one-kernel pass whose tiles find
-// their offsets by decoupled look-back measured slower at every size tried:
-// the chain of published prefixes, not the extra read of the keys, set its
-// pace.)  The element count and the number of significant key bits may live
-// on the device (the unique-based path only learns them there); passes beyond
-// the significant bits return at once, and the buffers are chosen so the last
-// active pass always writes the output.
+// The input may be cut into segments that are sorted independently and stay
+// in place.  The layer's sort uses one segment per table: the forward emits
+// each table's lookups contiguously, so sorting every table's segment on the
+// row id local to the table (row - row_base) sorts the global ids, with as
+// few digit passes as the largest table needs instead of the sum of all
+// tables' rows.  Skipped lookups (the sentinel id) take the all-ones local key
+// and the last pass moves them behind every valid id, so the output is
+// exactly the ascending sort of the global ids.
+//
+// Each pass runs over 3072-key tiles that never cross a segment: a per-tile
+// digit histogram (u16 counts, one contiguous row per tile), a scan of the
+// counts over groups of 16 tiles, a scan over each segment's groups that also
+// adds the segment's exclusive digit bases, and the stable in-tile ranking in
+// shared memory, whose coalesced runs go to segment start + digit base +
+// group offset + tile offset.  No tile waits on another.  The element count
+// and the number of significant key bits may live on the device (the
+// unique-based path only learns them there); passes beyond the significant
+// bits return at once, and the buffers are chosen so the last active pass
+// always writes the output.
 #include "emb_internal.cuh"
 
 namespace emb {
@@ -27,11 +36,12 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     return m;
 }
 
-// Exclusive sum over the block (blockDim.x == kSortThreads); `total` gets the sum.
+// Exclusive sum over the block (blockDim.x == NT); `total` gets the sum.
+template <int NT>
 __device__ __forceinline__ uint32_t block_exclusive_sum(uint32_t x, uint32_t* warp_buf, uint32_t* total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int kWarps = kSortThreads / 32;
+    constexpr int kWarps = NT / 32;
     uint32_t incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -58,188 +68,436 @@ __device__ __forceinline__ uint32_t block_exclusive_sum(uint32_t x, uint32_t* wa
     return r;
 }
 
+// Scratch of one sort (layout from sort_scratch_layout).
+struct SortScratch {
+    int64_t* seg_lo;        // [S] first position of each segment
+    int64_t* seg_len;       // [S]
+    int32_t* seg_tile0;     // [S+1] first tile of each segment; [S] = tiles in use
+    int32_t* seg_grp0;      // [S+1] first group of each segment; [S] = groups in use
+    uint32_t* skipcnt;      // [S] skipped ids per segment (last pass of the layer sort)
+    uint32_t* skippre;      // [S+1] their exclusive prefix; [S] = total
+    uint16_t* counts;       // [tiles][nb] per-tile digit counts, then in-group exclusive offsets
+    uint32_t* gsum;         // [groups][nb] per-group sums, then group offsets + segment digit bases
+    int4* tile_desc;        // [tiles] first position, length, segment, group of each tile in use
+    int4* grp_desc;         // [groups] first tile, tiles, segment of each group in use
+};
+
+// The per-pass context every kernel derives the same way from the device or
+// host element count and significant bits.
 struct PassCtx {
     int64_t n;
-    int64_t ntiles;
     int npe;       // effective passes
     bool active;
+    bool last;     // the last effective pass
     bool dst_out;  // this pass writes the output buffers
     bool src_in;   // this pass reads the input buffers
 };
 
-__device__ __forceinline__ PassCtx pass_ctx(int64_t n_host, const int64_t* n_dev, const int32_t* bits_dev,
-                                            int bits_max, int D, int pass, int tile)
+__device__ __forceinline__ PassCtx pass_ctx(const SortArgs& a, int pass)
 {
     PassCtx c;
-    int64_t n = n_host;
-    if (n_dev) {
-        int64_t m = *n_dev;
-        n = m < n_host ? (m < 0 ? 0 : m) : n_host;
+    int64_t n = a.n_host;
+    if (a.n_dev) {
+        const int64_t m = *a.n_dev;
+        n = m < a.n_host ? (m < 0 ? 0 : m) : a.n_host;
     }
     c.n = n;
-    c.ntiles = (n + tile - 1) / tile;
-    int b = bits_dev ? *bits_dev : bits_max;
+    int b = a.bits_dev ? *a.bits_dev : a.bits_max;
     if (b < 1) b = 1;
-    if (b > bits_max) b = bits_max;
-    c.npe = (b + D - 1) / D;
+    if (b > a.bits_max) b = a.bits_max;
+    c.npe = (b + a.D - 1) / a.D;
     c.active = pass < c.npe && n > 0;
+    c.last = pass == c.npe - 1;
     c.dst_out = ((c.npe - 1 - pass) & 1) == 0;
     c.src_in = pass == 0;
     return c;
 }
 
-// ---- one pass: three kernels (histogram per tile, scan, ranking) ----
+// Segment s holding tile (or group) index x of the prefix array p[0..S]: the s
+// with p[s] <= x < p[s+1] (empty segments skipped).
+__device__ __forceinline__ int find_seg(const int32_t* p, int S, int64_t x)
+{
+    int lo = 0, hi = S - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// The key a pass ranks: the input key, made local to its segment on the
+// first pass of the layer sort (all ones for a skipped or out-of-table id),
+// or with key_sub subtracted on the first pass of a plain sort.
+template <typename K>
+__device__ __forceinline__ K first_pass_key(const SortArgs& a, K k, int s, uint64_t sub)
+{
+    if (a.tables) {
+        const uint32_t g = (uint32_t)k;
+        const uint32_t rb = a.tables[s].row_base;
+        const uint64_t local = (uint64_t)g - rb;
+        return (g < a.sentinel && g >= rb && local < (uint64_t)a.tables[s].rows) ? (K)local : (K)a.skip_key;
+    }
+    return (K)(k - (K)sub);
+}
+
+// ---- segment and tile layout (one block) ----
+constexpr int kSetupThreads = 1024;
+
+__global__ void __launch_bounds__(kSetupThreads) sort_setup(SortArgs a, SortScratch sc)
+{
+    __shared__ uint32_t wbuf[kSetupThreads / 32 + 1];
+    __shared__ int64_t wmax[kSetupThreads / 32];
+    int64_t n = a.n_host;
+    if (a.n_dev) {
+        const int64_t m = *a.n_dev;
+        n = m < a.n_host ? (m < 0 ? 0 : m) : a.n_host;
+    }
+    const int S = a.num_seg;
+    const int per = (S + kSetupThreads - 1) / kSetupThreads;   // at most 4 (S <= 4096)
+    const int s0 = threadIdx.x * per;
+    // segment ends: the clamped offsets made non-decreasing (running maximum),
+    // the last one n, so the segments tile [0, n) exactly
+    int64_t hi[4];
+    int64_t run = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int s = s0 + q;
+        hi[q] = 0;
+        if (q < per && s < S) {
+            int64_t e = n;
+            if (a.offsets && s + 1 < S) {
+                e = a.offsets[(int64_t)(s + 1) * a.stride];
+                e = e < 0 ? 0 : (e > n ? n : e);
+            }
+            run = e > run ? e : run;
+            hi[q] = run;
+        }
+    }
+    // exclusive running maximum over threads
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t inc = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o && y > inc) inc = y;
+    }
+    if (lane == 31) wmax[warp] = inc;
+    __syncthreads();
+    int64_t before = __shfl_up_sync(0xffffffffu, inc, 1);
+    if (lane == 0) before = 0;
+    for (int w = 0; w < warp; ++w) before = wmax[w] > before ? wmax[w] : before;
+    uint32_t nt = 0, ng = 0;
+    int64_t lo = before;
+    uint32_t tl[4], gl[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int s = s0 + q;
+        tl[q] = gl[q] = 0;
+        if (q < per && s < S) {
+            const int64_t h = hi[q] > lo ? hi[q] : lo;
+            sc.seg_lo[s] = lo;
+            sc.seg_len[s] = h - lo;
+            tl[q] = (uint32_t)((h - lo + kSortTile - 1) / kSortTile);
+            gl[q] = (tl[q] + kSortGroupTiles - 1) / kSortGroupTiles;
+            nt += tl[q];
+            ng += gl[q];
+            lo = h;
+        }
+    }
+    uint32_t tot_t, tot_g;
+    uint32_t et = block_exclusive_sum<kSetupThreads>(nt, wbuf, &tot_t);
+    uint32_t eg = block_exclusive_sum<kSetupThreads>(ng, wbuf, &tot_g);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int s = s0 + q;
+        if (q < per && s < S) {
+            sc.seg_tile0[s] = (int32_t)et;
+            sc.seg_grp0[s] = (int32_t)eg;
+            et += tl[q];
+            eg += gl[q];
+        }
+    }
+    if (threadIdx.x == 0) {
+        sc.seg_tile0[S] = (int32_t)tot_t;
+        sc.seg_grp0[S] = (int32_t)tot_g;
+    }
+}
+
+// ---- one pass: histogram per tile, scans, ranking ----
 
 constexpr int kDownsweepBlocks = 4;   // resident blocks per SM the ranking kernel's registers are sized for
 
-template <typename K, int ITEMS>
-__global__ void __launch_bounds__(kSortThreads)
-sort_upsweep(const K* __restrict__ keys_in, const K* keys_out, const K* keys_tmp, int64_t n_host,
-             const int64_t* n_dev, const int32_t* bits_dev, int bits_max, int D, int pass,
-             const uint64_t* key_sub, uint32_t* __restrict__ counts)
+// Where every tile and group in use lies, one thread per tile (the segment of
+// a tile is a binary search over the segments' first tiles).
+__global__ void sort_tiles(SortArgs a, SortScratch sc, int64_t tiles_grid)
 {
-    constexpr int kTile = kSortThreads * ITEMS;
-    PassCtx c = pass_ctx(n_host, n_dev, bits_dev, bits_max, D, pass, kTile);
+    const int S = a.num_seg;
+    const int64_t ntiles = sc.seg_tile0[S];
+    for (int64_t tile = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; tile < ntiles && tile < tiles_grid;
+         tile += (int64_t)gridDim.x * blockDim.x) {
+        const int s = find_seg(sc.seg_tile0, S, tile);
+        const int64_t k = tile - sc.seg_tile0[s];
+        const int64_t start = sc.seg_lo[s] + k * (int64_t)kSortTile;
+        const int64_t rem = sc.seg_lo[s] + sc.seg_len[s] - start;
+        const int grp = sc.seg_grp0[s] + (int)(k / kSortGroupTiles);
+        sc.tile_desc[tile] = make_int4((int)start, rem < kSortTile ? (int)rem : kSortTile, s, grp);
+        if (k % kSortGroupTiles == 0) {
+            const int64_t left = sc.seg_tile0[s + 1] - tile;
+            sc.grp_desc[grp] = make_int4((int)tile, left < kSortGroupTiles ? (int)left : kSortGroupTiles, s, 0);
+        }
+    }
+}
+
+// Where tile `tile` lies: its segment, first position and element count.
+struct TileLoc {
+    int s;
+    int grp;
+    int64_t start;
+    int len;
+};
+
+__device__ __forceinline__ TileLoc locate_tile(const SortScratch& sc, int64_t tile)
+{
+    const int4 d = sc.tile_desc[tile];
+    TileLoc t;
+    t.start = d.x;
+    t.len = d.y;
+    t.s = d.z;
+    t.grp = d.w;
+    return t;
+}
+
+template <typename K>
+__global__ void __launch_bounds__(kSortThreads) sort_upsweep(SortArgs a, SortScratch sc, int pass)
+{
+    PassCtx c = pass_ctx(a, pass);
     const int64_t tile = blockIdx.x;
-    if (!c.active || tile >= c.ntiles) return;
-    const K* src = c.src_in ? keys_in : (c.dst_out ? keys_tmp : keys_out);
+    if (!c.active || tile >= sc.seg_tile0[a.num_seg]) return;
     __shared__ uint32_t hist[1 << kMaxDigitBits];
-    const int nb = 1 << D;
+    const int nb = 1 << a.D;
     for (int i = threadIdx.x; i < nb; i += kSortThreads) hist[i] = 0;
+    const TileLoc tl = locate_tile(sc, tile);
     __syncthreads();
-    const int shift = pass * D;
-    const K sub = (c.src_in && key_sub) ? (K)(*key_sub) : (K)0;
-    const int64_t base = tile * kTile;
+    const K* src = c.src_in ? static_cast<const K*>(a.keys_in)
+                            : (c.dst_out ? static_cast<const K*>(a.keys_tmp) : static_cast<const K*>(a.keys_out));
+    const int shift = pass * a.D;
+    const uint64_t sub = (c.src_in && a.key_sub) ? *a.key_sub : 0ull;
     const int lane = threadIdx.x & 31;
     // all of the thread's keys are requested before the first is counted
-    uint32_t dg[ITEMS];
+    uint32_t dg[kSortItems];
 #pragma unroll
-    for (int r = 0; r < ITEMS; ++r) {
-        const int64_t idx = base + (int64_t)r * kSortThreads + threadIdx.x;
-        dg[r] = idx < c.n ? (uint32_t)(((K)(src[idx] - sub) >> shift) & (K)(nb - 1)) : (uint32_t)nb;
+    for (int r = 0; r < kSortItems; ++r) {
+        const int e = r * kSortThreads + threadIdx.x;
+        dg[r] = (uint32_t)nb;
+        if (e < tl.len) {
+            K k = src[tl.start + e];
+            if (c.src_in) k = first_pass_key<K>(a, k, tl.s, sub);
+            dg[r] = (uint32_t)((k >> shift) & (K)(nb - 1));
+        }
     }
 #pragma unroll
-    for (int r = 0; r < ITEMS; ++r) {
+    for (int r = 0; r < kSortItems; ++r) {
         const uint32_t d = dg[r];
-        uint32_t peers = __match_any_sync(0xffffffffu, d);
-        int leader = __ffs(peers) - 1;
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        const int leader = __ffs(peers) - 1;
         if (lane == leader && d < (uint32_t)nb) atomicAdd(&hist[d], (uint32_t)__popc(peers));
     }
     __syncthreads();
-    for (int d = threadIdx.x; d < nb; d += kSortThreads) counts[(int64_t)d * c.ntiles + tile] = hist[d];
+    uint16_t* row = sc.counts + tile * (int64_t)nb;
+    for (int d = threadIdx.x; d < nb; d += kSortThreads) row[d] = (uint16_t)hist[d];
 }
 
-__global__ void __launch_bounds__(kSortThreads)
-sort_scan(uint32_t* __restrict__ counts, uint32_t* __restrict__ totals, int64_t n_host, const int64_t* n_dev,
-          const int32_t* bits_dev, int bits_max, int D, int pass, int tile_elems)
+// Per group of up to kSortGroupTiles tiles of one segment: each tile's count
+// becomes its exclusive offset within the group; gsum gets the group's sums.
+__global__ void __launch_bounds__(kSortThreads) sort_scan_groups(SortArgs a, SortScratch sc, int pass)
 {
-    PassCtx c = pass_ctx(n_host, n_dev, bits_dev, bits_max, D, pass, tile_elems);
-    const int d = blockIdx.x;
-    if (!c.active || d >= (1 << D)) return;
-    __shared__ uint32_t wbuf[kSortThreads / 32 + 1];
-    uint32_t* row = counts + (int64_t)d * c.ntiles;
-    uint32_t running = 0;
-    constexpr int kPer = 4;
-    for (int64_t base = 0; base < c.ntiles; base += (int64_t)kSortThreads * kPer) {
-        uint32_t v[kPer];
-        uint32_t s = 0;
-        const int64_t i0 = base + (int64_t)threadIdx.x * kPer;
+    PassCtx c = pass_ctx(a, pass);
+    const int64_t grp = blockIdx.x;
+    if (!c.active || grp >= sc.seg_grp0[a.num_seg]) return;
+    const int4 gd = sc.grp_desc[grp];
+    const int64_t t0 = gd.x;
+    const int nt = gd.y;
+    const int nb = 1 << a.D;
+    for (int d = threadIdx.x; d < nb; d += kSortThreads) {
+        uint32_t v[kSortGroupTiles];
 #pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-            v[q] = (i0 + q < c.ntiles) ? row[i0 + q] : 0u;
-            s += v[q];
-        }
-        uint32_t tot;
-        uint32_t ex = block_exclusive_sum(s, wbuf, &tot) + running;
+        for (int q = 0; q < kSortGroupTiles; ++q) v[q] = q < nt ? sc.counts[(t0 + q) * nb + d] : 0u;
+        uint32_t run = 0;
 #pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-            if (i0 + q < c.ntiles) row[i0 + q] = ex;
-            ex += v[q];
+        for (int q = 0; q < kSortGroupTiles; ++q) {
+            if (q < nt) sc.counts[(t0 + q) * nb + d] = (uint16_t)run;
+            run += v[q];
         }
-        running += tot;
+        sc.gsum[grp * nb + d] = run;
     }
-    if (threadIdx.x == 0) totals[d] = running;
 }
 
-template <typename K, int ITEMS>
-__global__ void __launch_bounds__(kSortThreads, kDownsweepBlocks)
-sort_downsweep(const K* __restrict__ keys_in, const uint32_t* __restrict__ vals_in, K* keys_out,
-               uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp, int64_t n_host, const int64_t* n_dev,
-               const int32_t* bits_dev, int bits_max, int D, int pass, const uint64_t* key_sub,
-               const uint32_t* __restrict__ counts, const uint32_t* __restrict__ totals)
+// Per segment: each group's sum becomes the group's exclusive offset within
+// the segment plus the segment's exclusive digit base; on the last pass of
+// the layer sort the segment's count of skipped ids (the all-ones top digit)
+// is recorded.
+__global__ void __launch_bounds__(kSortThreads) sort_scan_segments(SortArgs a, SortScratch sc, int pass)
 {
-    constexpr int kTile = kSortThreads * ITEMS;
-    PassCtx c = pass_ctx(n_host, n_dev, bits_dev, bits_max, D, pass, kTile);
+    PassCtx c = pass_ctx(a, pass);
+    const int s = blockIdx.x;
+    if (!c.active || s >= a.num_seg) return;
+    __shared__ uint32_t tot[1 << kMaxDigitBits];
+    __shared__ uint32_t wbuf[kSortThreads / 32 + 1];
+    const int nb = 1 << a.D;
+    const int64_t g0 = sc.seg_grp0[s], g1 = sc.seg_grp0[s + 1];
+    constexpr int kB = 8;   // group sums loaded per batch
+    for (int d = threadIdx.x; d < nb; d += kSortThreads) {
+        uint32_t run = 0;
+        for (int64_t g = g0; g < g1; g += kB) {
+            uint32_t v[kB];
+#pragma unroll
+            for (int q = 0; q < kB; ++q) v[q] = g + q < g1 ? sc.gsum[(g + q) * nb + d] : 0u;
+#pragma unroll
+            for (int q = 0; q < kB; ++q) {
+                if (g + q < g1) sc.gsum[(g + q) * nb + d] = run;
+                run += v[q];
+            }
+        }
+        tot[d] = run;
+    }
+    __syncthreads();
+    // exclusive scan of the segment's digit totals (a thread takes 4 consecutive digits)
+    uint32_t lt[4], sum = 0;
+    const int d0 = threadIdx.x * 4;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        lt[q] = d0 + q < nb ? tot[d0 + q] : 0u;
+        sum += lt[q];
+    }
+    uint32_t ex = block_exclusive_sum<kSortThreads>(sum, wbuf, nullptr);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (d0 + q < nb) tot[d0 + q] = ex;
+        ex += lt[q];
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < nb; d += kSortThreads) {
+        const uint32_t base = tot[d];
+        for (int64_t g = g0; g < g1; ++g) sc.gsum[g * nb + d] += base;
+    }
+    if (a.tables && c.last && threadIdx.x == 0) {
+        // skipped ids carry the largest digit, so everything before its base is valid
+        const uint32_t skipd = (uint32_t)(a.skip_key >> (pass * a.D)) & (uint32_t)(nb - 1);
+        sc.skipcnt[s] = (uint32_t)sc.seg_len[s] - tot[skipd];
+    }
+}
+
+// Exclusive prefix of the skipped ids over segments (last pass of the layer sort).
+__global__ void __launch_bounds__(kSetupThreads) sort_scan_skips(SortArgs a, SortScratch sc, int pass)
+{
+    PassCtx c = pass_ctx(a, pass);
+    if (!c.active || !c.last) return;
+    __shared__ uint32_t wbuf[kSetupThreads / 32 + 1];
+    const int S = a.num_seg;
+    const int per = (S + kSetupThreads - 1) / kSetupThreads;
+    const int s0 = threadIdx.x * per;
+    uint32_t v[4], sum = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[q] = (q < per && s0 + q < S) ? sc.skipcnt[s0 + q] : 0u;
+        sum += v[q];
+    }
+    uint32_t tot;
+    uint32_t ex = block_exclusive_sum<kSetupThreads>(sum, wbuf, &tot);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (q < per && s0 + q < S) sc.skippre[s0 + q] = ex;
+        ex += v[q];
+    }
+    if (threadIdx.x == 0) sc.skippre[S] = tot;
+}
+
+template <typename K>
+__global__ void __launch_bounds__(kSortThreads, kDownsweepBlocks) sort_downsweep(SortArgs a, SortScratch sc, int pass)
+{
+    PassCtx c = pass_ctx(a, pass);
     const int64_t tile = blockIdx.x;
-    if (!c.active || tile >= c.ntiles) return;
+    if (!c.active || tile >= sc.seg_tile0[a.num_seg]) return;
     const K* src_k;
     const uint32_t* src_v;
     K* dst_k;
     uint32_t* dst_v;
-    if (c.dst_out) { dst_k = keys_out; dst_v = vals_out; } else { dst_k = keys_tmp; dst_v = vals_tmp; }
-    if (c.src_in) { src_k = keys_in; src_v = vals_in; }
-    else if (c.dst_out) { src_k = keys_tmp; src_v = vals_tmp; }
-    else { src_k = keys_out; src_v = vals_out; }
+    if (c.dst_out) { dst_k = static_cast<K*>(a.keys_out); dst_v = a.vals_out; }
+    else { dst_k = static_cast<K*>(a.keys_tmp); dst_v = a.vals_tmp; }
+    if (c.src_in) { src_k = static_cast<const K*>(a.keys_in); src_v = a.vals_in; }
+    else if (c.dst_out) { src_k = static_cast<const K*>(a.keys_tmp); src_v = a.vals_tmp; }
+    else { src_k = static_cast<const K*>(a.keys_out); src_v = a.vals_out; }
 
     constexpr int kWarps = kSortThreads / 32;
-    const int nb = 1 << D;
+    const int nb = 1 << a.D;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     K* skey = reinterpret_cast<K*>(smem_raw);
-    uint32_t* sval = reinterpret_cast<uint32_t*>(skey + kTile);
-    uint32_t* wcnt = sval + kTile;                // [kWarps][nb]
-    uint32_t* tstart = wcnt + kWarps * nb;        // [nb]
+    uint32_t* sval = reinterpret_cast<uint32_t*>(skey + kSortTile);
+    uint32_t* tstart = sval + kSortTile;          // [nb]
     uint32_t* gbase = tstart + nb;                // [nb]
     uint32_t* wbuf = gbase + nb;                  // [kWarps + 1]
+    // per-warp digit counters: at most 32 * kSortItems per warp, so 16 bits
+    uint16_t* wcnt = reinterpret_cast<uint16_t*>(wbuf + kWarps + 1);   // [kWarps][nb]
 
-    for (int i = threadIdx.x; i < kWarps * nb; i += kSortThreads) wcnt[i] = 0;
-    __syncthreads();
+    for (int i = threadIdx.x; i < kWarps * nb / 2; i += kSortThreads) reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
+    const TileLoc tl = locate_tile(sc, tile);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int shift = pass * D;
-    const K sub = (c.src_in && key_sub) ? (K)(*key_sub) : (K)0;
-    const int64_t base = tile * kTile;
+    const int shift = pass * a.D;
+    const uint64_t sub = (c.src_in && a.key_sub) ? *a.key_sub : 0ull;
     const uint32_t lt = lanemask_lt();
-    // this thread's digits d0 .. d0+per-1 in the scans below: their totals and
-    // this tile's offsets within them are requested now, so the loads' latency
-    // passes behind the ranking
+    // this thread's digits d0 .. d0+3: where they go (segment start + digit
+    // base + group offset + tile offset) is requested now, so the loads'
+    // latency passes behind the ranking
     const int per = (nb + kSortThreads - 1) / kSortThreads;   // at most 4 (digits of at most 10 bits)
     const int d0 = threadIdx.x * per;
-    uint32_t lg_[4], lc_[4];
+    const int64_t grp = tl.grp;
+    uint32_t gb_[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        lg_[q] = 0u;
-        lc_[q] = 0u;
-        if (q < per && d0 + q < nb) {
-            lg_[q] = totals[d0 + q];
-            lc_[q] = counts[(int64_t)(d0 + q) * c.ntiles + tile];
-        }
+        gb_[q] = 0u;
+        if (q < per && d0 + q < nb)
+            gb_[q] = sc.gsum[grp * nb + d0 + q] + (uint32_t)sc.counts[tile * nb + d0 + q];
+    }
+    // the last pass of the layer sort puts skipped ids behind all valid ones
+    const bool relocate = a.tables && c.last;
+    uint32_t seg_base = (uint32_t)sc.seg_lo[tl.s];
+    uint32_t skip_base = 0, valid_in_seg = 0, skipd = 0xFFFFFFFFu;
+    if (relocate) {
+        skipd = (uint32_t)(a.skip_key >> shift) & (uint32_t)(nb - 1);
+        const uint32_t pre = sc.skippre[tl.s];
+        valid_in_seg = (uint32_t)sc.seg_len[tl.s] - sc.skipcnt[tl.s];
+        skip_base = (uint32_t)c.n - sc.skippre[a.num_seg] + pre;
+        seg_base -= pre;
     }
 
-    K k[ITEMS];
-    uint32_t v[ITEMS];
-    uint32_t dg[ITEMS];
-    uint32_t rk[ITEMS];
+    K k[kSortItems];
+    uint32_t v[kSortItems];
+    uint32_t dg[kSortItems];
+    uint32_t rk[kSortItems];
 #pragma unroll
-    for (int r = 0; r < ITEMS; ++r) {
-        const int e = warp * (ITEMS * 32) + r * 32 + lane;
-        const int64_t idx = base + e;
+    for (int r = 0; r < kSortItems; ++r) {
+        const int e = warp * (kSortItems * 32) + r * 32 + lane;
         dg[r] = (uint32_t)nb;
         k[r] = 0;
         v[r] = 0;
-        if (idx < c.n) {
-            k[r] = (K)(src_k[idx] - sub);
+        if (e < tl.len) {
+            const int64_t idx = tl.start + e;
+            k[r] = src_k[idx];
+            if (c.src_in) k[r] = first_pass_key<K>(a, k[r], tl.s, sub);
             v[r] = src_v ? src_v[idx] : (uint32_t)idx;
             dg[r] = (uint32_t)((k[r] >> shift) & (K)(nb - 1));
         }
     }
+    __syncthreads();   // the counters are cleared
 #pragma unroll
-    for (int r = 0; r < ITEMS; ++r) {
+    for (int r = 0; r < kSortItems; ++r) {
         uint32_t peers = __match_any_sync(0xffffffffu, dg[r]);
         int leader = __ffs(peers) - 1;
         uint32_t old = 0;
         if (lane == leader && dg[r] < (uint32_t)nb) {
             old = wcnt[warp * nb + dg[r]];
-            wcnt[warp * nb + dg[r]] = old + (uint32_t)__popc(peers);
+            wcnt[warp * nb + dg[r]] = (uint16_t)(old + (uint32_t)__popc(peers));
         }
         old = __shfl_sync(0xffffffffu, old, leader);
         rk[r] = old + (uint32_t)__popc(peers & lt);
@@ -248,41 +506,39 @@ sort_downsweep(const K* __restrict__ keys_in, const uint32_t* __restrict__ vals_
     __syncthreads();
     // per digit: exclusive prefix over warps and the tile total
     for (int d = threadIdx.x; d < nb; d += kSortThreads) {
-        uint32_t s = 0;
+        uint32_t sum = 0;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             uint32_t cnt = wcnt[w * nb + d];
-            wcnt[w * nb + d] = s;
-            s += cnt;
+            wcnt[w * nb + d] = (uint16_t)sum;
+            sum += cnt;
         }
-        tstart[d] = s;
+        tstart[d] = sum;
     }
     __syncthreads();
-    // exclusive scans over digits: tile-local starts and global digit bases
+    // exclusive scan over digits: tile-local starts; global bases from the scans
     {
-        uint32_t st = 0, sg = 0;
+        uint32_t st = 0;
         uint32_t lt_[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             lt_[q] = (q < per && d0 + q < nb) ? tstart[d0 + q] : 0u;
             st += lt_[q];
-            sg += lg_[q];
         }
-        uint32_t ext = block_exclusive_sum(st, wbuf, nullptr);
-        uint32_t exg = block_exclusive_sum(sg, wbuf, nullptr);
+        uint32_t ext = block_exclusive_sum<kSortThreads>(st, wbuf, nullptr);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            if (q < per && d0 + q < nb) {
-                tstart[d0 + q] = ext;
-                gbase[d0 + q] = exg + lc_[q];
+            const int d = d0 + q;
+            if (q < per && d < nb) {
+                tstart[d] = ext;
+                gbase[d] = (uint32_t)d == skipd ? skip_base + (gb_[q] - valid_in_seg) : seg_base + gb_[q];
             }
             ext += lt_[q];
-            exg += lg_[q];
         }
     }
     __syncthreads();
 #pragma unroll
-    for (int r = 0; r < ITEMS; ++r) {
+    for (int r = 0; r < kSortItems; ++r) {
         if (dg[r] < (uint32_t)nb) {
             uint32_t lp = tstart[dg[r]] + wcnt[warp * nb + dg[r]] + rk[r];
             skey[lp] = k[r];
@@ -290,92 +546,138 @@ sort_downsweep(const K* __restrict__ keys_in, const uint32_t* __restrict__ vals_
         }
     }
     __syncthreads();
-    const int64_t rem = c.n - base;
-    const int nvalid = rem < kTile ? (int)rem : kTile;
+    const uint32_t rb = a.tables ? a.tables[tl.s].row_base : 0u;
 #pragma unroll 4
-    for (int r = 0; r < ITEMS; ++r) {
+    for (int r = 0; r < kSortItems; ++r) {
         const int p = r * kSortThreads + threadIdx.x;
-        if (p < nvalid) {
+        if (p < tl.len) {
             K kk = skey[p];
-            uint32_t d = (uint32_t)((kk >> shift) & (K)(nb - 1));
-            int64_t o = (int64_t)gbase[d] + (p - (int64_t)tstart[d]);
+            const uint32_t d = (uint32_t)((kk >> shift) & (K)(nb - 1));
+            const int64_t o = (int64_t)gbase[d] + (p - (int64_t)tstart[d]);
+            // the layer sort's last pass writes global ids again
+            if (relocate) kk = d == skipd ? (K)a.sentinel : (K)(kk + rb);
             dst_k[o] = kk;
             dst_v[o] = sval[p];
         }
     }
 }
 
+// Byte offsets of the scratch arrays inside one region (host and device agree).
+struct ScratchLayout {
+    size_t seg_lo, seg_len, seg_tile0, seg_grp0, skipcnt, skippre, counts, gsum, tile_desc, grp_desc, total;
+};
+
+ScratchLayout scratch_layout(const SortPlan& p)
+{
+    ScratchLayout l{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) & ~size_t(255);
+        return at;
+    };
+    const size_t S = (size_t)p.num_seg_max;
+    const size_t nb = (size_t)1 << p.digit_bits;
+    l.seg_lo = take(8 * S);
+    l.seg_len = take(8 * S);
+    l.seg_tile0 = take(4 * (S + 1));
+    l.seg_grp0 = take(4 * (S + 1));
+    l.skipcnt = take(4 * S);
+    l.skippre = take(4 * (S + 1));
+    l.counts = take(2 * nb * (size_t)p.tiles_max);
+    l.gsum = take(4 * nb * (size_t)p.groups_max);
+    l.tile_desc = take(16 * (size_t)p.tiles_max);
+    l.grp_desc = take(16 * (size_t)p.groups_max);
+    l.total = off;
+    return l;
+}
+
 }  // namespace
 
-SortPlan make_sort_plan(int64_t n_max, int bits_max)
+SortPlan make_sort_plan(int64_t n_max, int bits_max, int num_seg_max)
 {
     SortPlan p;
     if (bits_max < 1) bits_max = 1;
+    if (num_seg_max < 1) num_seg_max = 1;
     p.n_max = n_max;
+    p.num_seg_max = num_seg_max;
     p.bits_max = bits_max;
     p.passes_max = (bits_max + kMaxDigitBits - 1) / kMaxDigitBits;
     p.digit_bits = (bits_max + p.passes_max - 1) / p.passes_max;
-    p.tiles_max = (n_max + kSortThreads * kSortItems - 1) / (kSortThreads * kSortItems);
-    if (p.tiles_max < 1) p.tiles_max = 1;
-    p.counts_bytes = sizeof(uint32_t) * ((size_t)1 << p.digit_bits) * (size_t)p.tiles_max;
-    p.totals_bytes = sizeof(uint32_t) * ((size_t)1 << p.digit_bits);
+    p.tiles_max = (n_max + kSortTile - 1) / kSortTile + num_seg_max;
+    p.groups_max = p.tiles_max / kSortGroupTiles + num_seg_max;
+    p.scratch_bytes = scratch_layout(p).total;
     return p;
 }
 
-template <typename K, int ITEMS>
-static size_t downsweep_smem(int D)
+int table_sort_bits(int64_t rows_max)
 {
-    const int nb = 1 << D;
-    return (size_t)kSortThreads * ITEMS * (sizeof(K) + sizeof(uint32_t)) +
-           sizeof(uint32_t) * ((size_t)(kSortThreads / 32) * nb + 2 * (size_t)nb + kSortThreads / 32 + 1);
+    // local ids 0 .. rows_max - 1 plus the all-ones key of skipped lookups,
+    // whose top digit no valid id may share
+    int b = 1;
+    while (b < 63 && ((uint64_t)rows_max >> b) != 0) ++b;
+    for (;; ++b) {
+        const int passes = (b + kMaxDigitBits - 1) / kMaxDigitBits;
+        const int D = (b + passes - 1) / passes;
+        const int top_shift = (passes - 1) * D;
+        const uint64_t top_skip = (((uint64_t)1 << b) - 1) >> top_shift;
+        if ((((uint64_t)rows_max - 1) >> top_shift) < top_skip) return b;
+    }
 }
 
-template <typename K, int ITEMS>
-static int sort_passes_3k(const SortPlan& plan, const K* keys_in, const uint32_t* vals_in, K* keys_out,
-                          uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp, uint32_t* counts, uint32_t* totals,
-                          int64_t n_host, const int64_t* n_dev, const int32_t* bits_dev, const uint64_t* key_sub,
-                          cudaStream_t st)
+template <typename K>
+int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream_t st)
 {
-    constexpr int kTile = kSortThreads * ITEMS;
-    const int D = plan.digit_bits;
-    const int64_t tiles = (n_host + kTile - 1) / kTile;
-    const size_t smem = downsweep_smem<K, ITEMS>(D);
-    if (cudaFuncSetAttribute(sort_downsweep<K, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    if (a.n_host <= 0) return 0;
+    if (a.num_seg < 1 || a.num_seg > plan.num_seg_max || a.n_host > plan.n_max || (a.tables && sizeof(K) != 4))
         return -1;
-    int launched = 0;
+    a.bits_max = plan.bits_max;
+    a.D = plan.digit_bits;
+    a.skip_key = ((uint64_t)1 << plan.bits_max) - 1;
+    const ScratchLayout l = scratch_layout(plan);
+    char* base = static_cast<char*>(scratch);
+    SortScratch sc;
+    sc.seg_lo = reinterpret_cast<int64_t*>(base + l.seg_lo);
+    sc.seg_len = reinterpret_cast<int64_t*>(base + l.seg_len);
+    sc.seg_tile0 = reinterpret_cast<int32_t*>(base + l.seg_tile0);
+    sc.seg_grp0 = reinterpret_cast<int32_t*>(base + l.seg_grp0);
+    sc.skipcnt = reinterpret_cast<uint32_t*>(base + l.skipcnt);
+    sc.skippre = reinterpret_cast<uint32_t*>(base + l.skippre);
+    sc.counts = reinterpret_cast<uint16_t*>(base + l.counts);
+    sc.gsum = reinterpret_cast<uint32_t*>(base + l.gsum);
+    sc.tile_desc = reinterpret_cast<int4*>(base + l.tile_desc);
+    sc.grp_desc = reinterpret_cast<int4*>(base + l.grp_desc);
+
+    const int64_t tiles = (a.n_host + kSortTile - 1) / kSortTile + a.num_seg;
+    const int64_t groups = tiles / kSortGroupTiles + a.num_seg;
+    const int nb = 1 << plan.digit_bits;
+    const size_t smem = (size_t)kSortTile * (sizeof(K) + sizeof(uint32_t)) +
+                        sizeof(uint32_t) * (2 * (size_t)nb + kSortThreads / 32 + 1) +
+                        sizeof(uint16_t) * (size_t)(kSortThreads / 32) * nb;
+    if (cudaFuncSetAttribute(sort_downsweep<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return -1;
+    sort_setup<<<1, kSetupThreads, 0, st>>>(a, sc);
+    const unsigned tile_blocks = (unsigned)((tiles + 255) / 256);
+    sort_tiles<<<tile_blocks, 256, 0, st>>>(a, sc, tiles);
+    int launched = 2;
     for (int p = 0; p < plan.passes_max; ++p) {
-        sort_upsweep<K, ITEMS><<<(unsigned)tiles, kSortThreads, 0, st>>>(keys_in, keys_out, keys_tmp, n_host, n_dev,
-                                                                         bits_dev, plan.bits_max, D, p, key_sub,
-                                                                         counts);
-        sort_scan<<<1u << D, kSortThreads, 0, st>>>(counts, totals, n_host, n_dev, bits_dev, plan.bits_max, D, p,
-                                                    kTile);
-        sort_downsweep<K, ITEMS><<<(unsigned)tiles, kSortThreads, smem, st>>>(
-            keys_in, vals_in, keys_out, vals_out, keys_tmp, vals_tmp, n_host, n_dev, bits_dev, plan.bits_max, D,
-            p, key_sub, counts, totals);
+        sort_upsweep<K><<<(unsigned)tiles, kSortThreads, 0, st>>>(a, sc, p);
+        sort_scan_groups<<<(unsigned)groups, kSortThreads, 0, st>>>(a, sc, p);
+        sort_scan_segments<<<(unsigned)a.num_seg, kSortThreads, 0, st>>>(a, sc, p);
         launched += 3;
+        if (a.tables) {
+            sort_scan_skips<<<1, kSetupThreads, 0, st>>>(a, sc, p);
+            ++launched;
+        }
+        sort_downsweep<K><<<(unsigned)tiles, kSortThreads, smem, st>>>(a, sc, p);
+        ++launched;
     }
     if (cudaGetLastError() != cudaSuccess) return -1;
     return launched;
 }
 
-template <typename K>
-int radix_sort_pairs(const SortPlan& plan, const K* keys_in, const uint32_t* vals_in, K* keys_out,
-                     uint32_t* vals_out, K* keys_tmp, uint32_t* vals_tmp, uint32_t* counts, uint32_t* totals,
-                     int64_t n_host, const int64_t* n_dev, const int32_t* bits_dev, const uint64_t* key_sub,
-                     cudaStream_t st)
-{
-    if (n_host <= 0) return 0;
-    return sort_passes_3k<K, kSortItems>(plan, keys_in, vals_in, keys_out, vals_out, keys_tmp, vals_tmp, counts,
-                                         totals, n_host, n_dev, bits_dev, key_sub, st);
-}
-
-template int radix_sort_pairs<uint32_t>(const SortPlan&, const uint32_t*, const uint32_t*, uint32_t*, uint32_t*,
-                                        uint32_t*, uint32_t*, uint32_t*, uint32_t*, int64_t, const int64_t*,
-                                        const int32_t*, const uint64_t*, cudaStream_t);
-template int radix_sort_pairs<uint64_t>(const SortPlan&, const uint64_t*, const uint32_t*, uint64_t*, uint32_t*,
-                                        uint64_t*, uint32_t*, uint32_t*, uint32_t*, int64_t, const int64_t*,
-                                        const int32_t*, const uint64_t*, cudaStream_t);
+template int radix_sort_pairs<uint32_t>(const SortPlan&, SortArgs, void*, cudaStream_t);
+template int radix_sort_pairs<uint64_t>(const SortPlan&, SortArgs, void*, cudaStream_t);
 
 // ---------------------------------------------------------------------------
 // run-length encoding of sorted keys
@@ -402,7 +704,7 @@ rle_count(const K* __restrict__ sk, int64_t n, uint64_t key_max, uint32_t* __res
         if (p < n && is_head(sk, p, key_max)) ++c;
     }
     uint32_t tot;
-    block_exclusive_sum(c, wbuf, &tot);
+    block_exclusive_sum<kRleThreads>(c, wbuf, &tot);
     if (threadIdx.x == 0) tile_cnt[blockIdx.x] = tot;
 }
 
@@ -421,7 +723,7 @@ rle_scan(uint32_t* __restrict__ tile_cnt, int64_t ntiles, int64_t n, int32_t* __
             s += v[q];
         }
         uint32_t tot;
-        uint32_t ex = block_exclusive_sum(s, wbuf, &tot) + running;
+        uint32_t ex = block_exclusive_sum<kRleThreads>(s, wbuf, &tot) + running;
         for (int q = 0; q < kPer; ++q) {
             if (i0 + q < ntiles) tile_cnt[i0 + q] = ex;
             ex += v[q];
@@ -454,7 +756,7 @@ rle_write(const K* __restrict__ sk, const uint32_t* __restrict__ vals, int64_t n
         h[q] = p < n && is_head(sk, p, key_max);
         c += h[q];
     }
-    uint32_t s = block_exclusive_sum(c, wbuf, nullptr) + tile_base[blockIdx.x];
+    uint32_t s = block_exclusive_sum<kRleThreads>(c, wbuf, nullptr) + tile_base[blockIdx.x];
     const uint64_t add = key_add ? *key_add : 0ull;
     const uint32_t U = (uint32_t)*num_unique;
     // s counts heads strictly before this thread's first element; the run of

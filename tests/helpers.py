@@ -101,6 +101,9 @@ def run_gpu_step(w: ci.Workload, batch: ci.Batch, grad: np.ndarray, variant: str
     dev = torch.device("cuda", 0)
     layer = EmbeddingLayer(w.tables, w.batch, max(batch.nnz, 1) if max_nnz is None else max_nnz)
     layer.init_uniform(seed, w.w_lo, w.w_hi)
+    # the dedup by-products are kept from the start: with early dedup the
+    # forward already runs the dedup
+    layer.set_keep_dedup(True)
     if early:
         layer.set_early_dedup(variant)
     keys = torch.from_numpy(batch.keys).to(dev)
@@ -110,7 +113,6 @@ def run_gpu_step(w: ci.Workload, batch: ci.Batch, grad: np.ndarray, variant: str
     out = layer.forward(keys, offsets, tids, batch.batch)
     st_f = layer.sync_status()
     out_np = out.cpu().numpy()
-    layer.set_keep_dedup(True)
     layer.backward_update(g, variant)
     st_b = layer.sync_status()
     u, inv, cnt, seg, bags = layer.dedup_result(with_inverse=variant != "reduction")

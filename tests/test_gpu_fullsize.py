@@ -88,7 +88,7 @@ def test_fullsize_sampled_parity(name, variant):
         full_inv[pos] = inv_s
         ref_out, ref_scale = oracle.forward(w.tables, B, batch.offsets, full_inv, store, bags=bags, want_scale=True)
         assert max_rel_err(out_s, ref_out[bsample], ref_scale[bsample]) <= 1e-5
-        report_plain("%s/%s full size" % (name, variant), "forward", out_s, ref_out[bsample])
+        assert report_plain("%s/%s full size" % (name, variant), "forward", out_s, ref_out[bsample]) <= 1e-5
 
         # ---- dedup: properties that fix the result uniquely ----
         valid = gids >= 0

@@ -233,14 +233,136 @@ __device__ __forceinline__ void pool_bags(const FwdArgs& a, const TableDev& tb, 
     }
 }
 
+// Rows requested ahead through shared memory: each lane copies its 16 bytes
+// (8 for 16-bit rows) of a row straight from memory into its own slot of a
+// ring of kRing slots (cp.async, no registers held while the copy is in
+// flight) and reads them back when the row is added.  Slot r of thread x is
+// at ((r * kThreads) + x) * SLOT bytes (SLOT = 16, or 8 where every table
+// stores 16-bit rows), so a warp's reads of a slot are conflict-free; no lane
+// ever reads another lane's slots.
+constexpr int kRing = 16;   // slots per lane: two batches of eight rows
+
+// Shared memory of one block's rings: slots of 16 bytes, or 8 in the kernel
+// for layers whose tables all store 16-bit rows.
+constexpr int ring_bytes(int slot_bytes) { return kRing * kThreads * slot_bytes; }
+
+__device__ __forceinline__ void ring_copy(uint32_t dst, const char* src, bool f32, bool live)
+{
+    // a skipped key or a position past the bag fills its slot with zeros (nothing
+    // is read); copies go through L1, which keeps the hottest rows of skewed keys
+    const int n = live ? (f32 ? 16 : 8) : 0;
+    if (f32)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void ring_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void ring_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// pool_bags for the training forward, with the rows of a window's keys
+// travelling through the lane's shared-memory ring: the next batch of eight
+// rows is requested before the current batch is added, so up to sixteen rows
+// per lane are in flight.
+template <int LR, int DT, int SLOT>
+__device__ __forceinline__ void pool_bags_ring(const FwdArgs& a, const TableDev& tb, const int64_t* kp, int li,
+                                               uint32_t gmask, int64_t j0, int nbg, int my_start, int my_end,
+                                               bool my_tid_ok, bool colok, float* out_col, int64_t bg0,
+                                               uint32_t ring)
+{
+    constexpr int KPL = LR >= 4 ? 32 / LR : 8;   // keys each lane loads per window
+    constexpr int WIN = KPL * LR;                // keys per window
+    constexpr bool F32 = DT == EMB_F32;
+    const char* wlane = static_cast<const char*>(tb.w) + (F32 ? 16 : 8) * li;
+    const uint32_t rbytes = (uint32_t)tb.dim * (F32 ? 4u : 2u);
+    const bool mean = tb.pooling == EMB_POOL_MEAN;
+    static_assert(!F32 || SLOT == 16, "fp32 rows need 16-byte slots");
+    constexpr uint32_t kSlot = kThreads * SLOT;  // bytes between a lane's consecutive slots
+    for (int k = 0; k < nbg; ++k) {
+        const int s0 = __shfl_sync(gmask, my_start, k, LR);
+        const int e0 = __shfl_sync(gmask, my_end, k, LR);
+        const bool tok = __shfl_sync(gmask, my_tid_ok, k, LR);
+        float2 sa = make_float2(0.f, 0.f), sb = sa, ca = sa, cb = sa;
+        for (int w = s0; w < e0; w += WIN) {
+            uint32_t kk[KPL];
+#pragma unroll
+            for (int j = 0; j < KPL; ++j) {
+                const int p = w + li + j * LR;
+                kk[j] = kNoRow;
+                if (p < e0) {
+                    const int64_t key = __ldg(kp + p);
+                    const bool valid = tok && key >= 0 && key < tb.rows;
+                    if (a.write_ids) {
+                        a.gid_out[p] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
+                        a.bag_out[p] = (uint32_t)(j0 + k);
+                    }
+                    if (!valid && tok) atomicOr(a.err, ERRBIT_KEY_RANGE);
+                    if (valid) kk[j] = (uint32_t)key;
+                }
+            }
+            const int n = e0 - w < WIN ? e0 - w : WIN;
+            // batch b (keys 8b .. 8b+7 of the window) goes to slots 8*(b&1) ..
+            auto request = [&](int b) {
+#pragma unroll
+                for (int u = 0; u < kPrefetch; ++u) {
+                    const int q = b * kPrefetch + u;
+                    const uint32_t kq = __shfl_sync(gmask, kk[q / LR], q % LR, LR);
+                    const bool live = q < n && kq != kNoRow && colok;
+                    ring_copy(ring + (uint32_t)((b & 1) * kPrefetch + u) * kSlot,
+                              live ? wlane + (uint64_t)kq * rbytes : wlane, F32, live);
+                }
+                ring_commit();
+            };
+            const int nb = (n + kPrefetch - 1) / kPrefetch;
+            request(0);
+            for (int b = 0; b < nb; ++b) {
+                if (b + 1 < nb) request(b + 1);
+                else ring_commit();       // an empty group keeps "all but the newest" meaning batch b
+                ring_wait_one();
+                const uint32_t base = ring + (uint32_t)((b & 1) * kPrefetch) * kSlot;
+#pragma unroll
+                for (int u = 0; u < kPrefetch; ++u) {
+                    float4 x;
+                    if constexpr (F32) {
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                                     : "r"(base + (uint32_t)u * kSlot));
+                    } else {
+                        uint2 r;
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(base + (uint32_t)u * kSlot));
+                        x = bits16_to_f32(r, DT);
+                    }
+                    // slots of positions past the bag or of skipped keys hold zeros,
+                    // which leave the sum unchanged
+                    sum2_add(sa, ca, make_float2(x.x, x.y));
+                    sum2_add(sb, cb, make_float2(x.z, x.w));
+                }
+            }
+        }
+        const float2 ra = add2(sa, ca), rb = add2(sb, cb);
+        float4 r = make_float4(ra.x, ra.y, rb.x, rb.y);
+        const int L = e0 - s0;
+        if (mean && L > 0) {
+            const float fl = (float)L;
+            r = make_float4(__fdiv_rn(r.x, fl), __fdiv_rn(r.y, fl), __fdiv_rn(r.z, fl), __fdiv_rn(r.w, fl));
+        }
+        if (colok) __stcs(reinterpret_cast<float4*>(out_col + (bg0 + k) * a.ld), r);
+    }
+}
+
 // The pooling of multi-key bags for a table of row width Lr lanes and
 // storage type dt.
-template <bool kInfer, int DT>
+template <bool kInfer, int DT, int SLOT>
 __device__ __forceinline__ void pool_bags_lr(int Lr, const FwdArgs& a, const TableDev& tb, const int64_t* kp, int li,
                                              uint32_t gmask, int64_t j0, int nbg, int my_start, int my_end,
-                                             bool my_tid_ok, bool colok, float* out_col, int64_t bg0)
+                                             bool my_tid_ok, bool colok, float* out_col, int64_t bg0, uint32_t ring)
 {
-#define POOL(LR) pool_bags<LR, kInfer, DT>(a, tb, kp, li, gmask, j0, nbg, my_start, my_end, my_tid_ok, colok, out_col, bg0)
+#define POOL(LR)                                                                                                     \
+    if constexpr (kInfer)                                                                                            \
+        pool_bags<LR, kInfer, DT>(a, tb, kp, li, gmask, j0, nbg, my_start, my_end, my_tid_ok, colok, out_col, bg0); \
+    else                                                                                                             \
+        pool_bags_ring<LR, DT, SLOT>(a, tb, kp, li, gmask, j0, nbg, my_start, my_end, my_tid_ok, colok, out_col, bg0, \
+                                     ring)
     switch (Lr) {
         case 1: POOL(1); break;
         case 2: POOL(2); break;
@@ -264,6 +386,9 @@ constexpr int kBlocks16 = 4;   // resident blocks of the kernel for layers of 16
 template <int kMinBlocks, bool kInfer>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
 {
+    constexpr int kSlotBytes = kMinBlocks == kBlocks16 ? 8 : 16;
+    extern __shared__ __align__(16) unsigned char fwd_ring[];   // the training forward's row rings
+    const uint32_t ring = (uint32_t)__cvta_generic_to_shared(fwd_ring) + threadIdx.x * kSlotBytes;
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int t = (int)(gw / a.warps_per_table);
@@ -357,16 +482,21 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
 
     // several keys per bag: the group pools its bags one after another
     // positions fit in 32 bits (lanes past the group's bags are never read)
-    // the kernel for layers whose tables all store 16-bit rows has no fp32 path
-    if (kMinBlocks != kBlocks16 && tb.dtype == EMB_F32)
-        pool_bags_lr<kInfer, EMB_F32>(Lr, a, tb, kp, li, gmask, j0, nbg, (int)my_start, (int)my_end, my_tid_ok, colok,
-                                      out_col, bg0);
-    else if (tb.dtype == EMB_F16)
-        pool_bags_lr<kInfer, EMB_F16>(Lr, a, tb, kp, li, gmask, j0, nbg, (int)my_start, (int)my_end, my_tid_ok, colok,
-                                      out_col, bg0);
+    const int s32 = (int)my_start, e32 = (int)my_end;
+    if constexpr (kMinBlocks != kBlocks16) {
+        if (tb.dtype == EMB_F32) {
+            pool_bags_lr<kInfer, EMB_F32, kSlotBytes>(Lr, a, tb, kp, li, gmask, j0, nbg, s32, e32, my_tid_ok, colok,
+                                                      out_col, bg0, ring);
+            return;
+        }
+    }
+    // (the kernel for layers whose tables all store 16-bit rows has no fp32 path)
+    if (tb.dtype == EMB_F16)
+        pool_bags_lr<kInfer, EMB_F16, kSlotBytes>(Lr, a, tb, kp, li, gmask, j0, nbg, s32, e32, my_tid_ok, colok, out_col,
+                                                  bg0, ring);
     else
-        pool_bags_lr<kInfer, EMB_BF16>(Lr, a, tb, kp, li, gmask, j0, nbg, (int)my_start, (int)my_end, my_tid_ok,
-                                       colok, out_col, bg0);
+        pool_bags_lr<kInfer, EMB_BF16, kSlotBytes>(Lr, a, tb, kp, li, gmask, j0, nbg, s32, e32, my_tid_ok, colok,
+                                                   out_col, bg0, ring);
 }
 
 // Global row id and bag of every lookup, nothing else: the forward's id
@@ -439,10 +569,12 @@ int launch_forward(const FwdArgs& a, cudaStream_t st)
         else
             fwd_pool<3, true><<<blocks, kThreads, 0, st>>>(a);
     } else {
-        if (a.rows16)
-            fwd_pool<kBlocks16, false><<<blocks, kThreads, 0, st>>>(a);
-        else
-            fwd_pool<3, false><<<blocks, kThreads, 0, st>>>(a);
+        auto kernel = a.rows16 ? fwd_pool<kBlocks16, false> : fwd_pool<3, false>;
+        const int smem = ring_bytes(a.rows16 ? 8 : 16);
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+            return -1;
+        kernel<<<blocks, kThreads, smem, st>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }

@@ -225,6 +225,22 @@ __global__ void __launch_bounds__(kSetupThreads) sort_setup(SortArgs a, SortScra
 
 // ---- one pass: histogram per tile, scans, ranking ----
 
+// Bytes of the ranking kernel's first shared region: the per-warp digit masks
+// while ranking; then the block scans' warp sums (behind the tile's place);
+// then the tile's keys and values in their in-tile sorted order.
+__host__ __device__ __forceinline__ size_t sort_tile_bytes(size_t key_bytes)
+{
+    return ((size_t)kSortTile * (key_bytes + sizeof(uint32_t)) + 15) & ~size_t(15);
+}
+
+__host__ __device__ __forceinline__ size_t sort_region0_bytes(size_t key_bytes, int nb)
+{
+    const size_t masks = sizeof(uint32_t) * (size_t)(kSortThreads / 32) * (size_t)nb;
+    const size_t tile = sort_tile_bytes(key_bytes) + 64;
+    const size_t r = masks > tile ? masks : tile;
+    return (r + 15) & ~size_t(15);
+}
+
 constexpr int kDownsweepBlocks = 4;   // resident blocks per SM the ranking kernel's registers are sized for
 
 // Where every tile and group in use lies, one thread per tile (the segment of
@@ -282,7 +298,6 @@ __global__ void __launch_bounds__(kSortThreads) sort_upsweep(SortArgs a, SortScr
                             : (c.dst_out ? static_cast<const K*>(a.keys_tmp) : static_cast<const K*>(a.keys_out));
     const int shift = pass * a.D;
     const uint64_t sub = (c.src_in && a.key_sub) ? *a.key_sub : 0ull;
-    const int lane = threadIdx.x & 31;
     // all of the thread's keys are requested before the first is counted
     uint32_t dg[kSortItems];
 #pragma unroll
@@ -295,13 +310,10 @@ __global__ void __launch_bounds__(kSortThreads) sort_upsweep(SortArgs a, SortScr
             dg[r] = (uint32_t)((k >> shift) & (K)(nb - 1));
         }
     }
+    // shared-memory atomics are cheap even where many lanes hit one digit
 #pragma unroll
-    for (int r = 0; r < kSortItems; ++r) {
-        const uint32_t d = dg[r];
-        const uint32_t peers = __match_any_sync(0xffffffffu, d);
-        const int leader = __ffs(peers) - 1;
-        if (lane == leader && d < (uint32_t)nb) atomicAdd(&hist[d], (uint32_t)__popc(peers));
-    }
+    for (int r = 0; r < kSortItems; ++r)
+        if (dg[r] < (uint32_t)nb) atomicAdd(&hist[dg[r]], 1u);
     __syncthreads();
     uint16_t* row = sc.counts + tile * (int64_t)nb;
     for (int d = threadIdx.x; d < nb; d += kSortThreads) row[d] = (uint16_t)hist[d];
@@ -431,15 +443,20 @@ __global__ void __launch_bounds__(kSortThreads, kDownsweepBlocks) sort_downsweep
     constexpr int kWarps = kSortThreads / 32;
     const int nb = 1 << a.D;
     extern __shared__ __align__(16) unsigned char smem_raw[];
+    // region 0: while ranking, per-warp lane masks of each digit; then the
+    // tile's keys and values in their in-tile sorted order
+    uint32_t* wmask = reinterpret_cast<uint32_t*>(smem_raw);   // [kWarps][nb]
     K* skey = reinterpret_cast<K*>(smem_raw);
     uint32_t* sval = reinterpret_cast<uint32_t*>(skey + kSortTile);
-    uint32_t* tstart = sval + kSortTile;          // [nb]
+    unsigned char* region1 = smem_raw + sort_region0_bytes(sizeof(K), nb);
+    uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem_raw + sort_tile_bytes(sizeof(K)));   // [kWarps + 1]
+    uint32_t* tstart = reinterpret_cast<uint32_t*>(region1);   // [nb]
     uint32_t* gbase = tstart + nb;                // [nb]
-    uint32_t* wbuf = gbase + nb;                  // [kWarps + 1]
     // per-warp digit counters: at most 32 * kSortItems per warp, so 16 bits
-    uint16_t* wcnt = reinterpret_cast<uint16_t*>(wbuf + kWarps + 1);   // [kWarps][nb]
+    uint16_t* wcnt = reinterpret_cast<uint16_t*>(gbase + nb);   // [kWarps][nb]
 
     for (int i = threadIdx.x; i < kWarps * nb / 2; i += kSortThreads) reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
+    for (int i = threadIdx.x; i < kWarps * nb; i += kSortThreads) wmask[i] = 0u;
     const TileLoc tl = locate_tile(sc, tile);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -489,18 +506,30 @@ __global__ void __launch_bounds__(kSortThreads, kDownsweepBlocks) sort_downsweep
             dg[r] = (uint32_t)((k[r] >> shift) & (K)(nb - 1));
         }
     }
-    __syncthreads();   // the counters are cleared
+    __syncthreads();   // the counters and masks are cleared
+    // stable rank of each item among the warp's items of its digit: the lanes
+    // of one step that share a digit find each other through an atomic OR of
+    // their lane bits into the digit's mask; the lowest of them advances the
+    // digit's counter and clears the mask
+    uint32_t* mymask = wmask + warp * nb;
+    uint16_t* mycnt = wcnt + warp * nb;
 #pragma unroll
     for (int r = 0; r < kSortItems; ++r) {
-        uint32_t peers = __match_any_sync(0xffffffffu, dg[r]);
-        int leader = __ffs(peers) - 1;
-        uint32_t old = 0;
-        if (lane == leader && dg[r] < (uint32_t)nb) {
-            old = wcnt[warp * nb + dg[r]];
-            wcnt[warp * nb + dg[r]] = (uint16_t)(old + (uint32_t)__popc(peers));
+        const uint32_t d = dg[r];
+        const bool in = d < (uint32_t)nb;
+        if (in) atomicOr(mymask + d, 1u << lane);
+        __syncwarp();
+        uint32_t peers = 0, base = 0;
+        if (in) {
+            peers = mymask[d];
+            base = mycnt[d];
         }
-        old = __shfl_sync(0xffffffffu, old, leader);
-        rk[r] = old + (uint32_t)__popc(peers & lt);
+        __syncwarp();
+        if (in && lane == __ffs(peers) - 1) {
+            mycnt[d] = (uint16_t)(base + (uint32_t)__popc(peers));
+            mymask[d] = 0u;
+        }
+        rk[r] = base + (uint32_t)__popc(peers & lt);
         __syncwarp();
     }
     __syncthreads();
@@ -651,10 +680,10 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
     const int64_t tiles = (a.n_host + kSortTile - 1) / kSortTile + a.num_seg;
     const int64_t groups = tiles / kSortGroupTiles + a.num_seg;
     const int nb = 1 << plan.digit_bits;
-    const size_t smem = (size_t)kSortTile * (sizeof(K) + sizeof(uint32_t)) +
-                        sizeof(uint32_t) * (2 * (size_t)nb + kSortThreads / 32 + 1) +
+    const size_t smem = sort_region0_bytes(sizeof(K), nb) + sizeof(uint32_t) * 2 * (size_t)nb +
                         sizeof(uint16_t) * (size_t)(kSortThreads / 32) * nb;
-    if (cudaFuncSetAttribute(sort_downsweep<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(sort_downsweep<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(sort_downsweep<K>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
         return -1;
     sort_setup<<<1, kSetupThreads, 0, st>>>(a, sc);
     const unsigned tile_blocks = (unsigned)((tiles + 255) / 256);

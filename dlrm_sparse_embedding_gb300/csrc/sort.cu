@@ -225,6 +225,11 @@ __global__ void __launch_bounds__(kSetupThreads) sort_setup(SortArgs a, SortScra
 
 // ---- one pass: histogram per tile, scans, ranking ----
 
+constexpr int kDownsweepBlocks = 2;   // resident (persistent) blocks per SM of the ranking kernel
+constexpr int kDownThreads = 256;      // ranking block: 8 warps ...
+constexpr int kDownItems = kSortTile / kDownThreads;   // ... of 12 items each per tile
+static_assert(kDownItems * kDownThreads == kSortTile, "the ranking block covers one tile");
+
 // Bytes of the ranking kernel's first shared region: the per-warp digit masks
 // while ranking; then the block scans' warp sums (behind the tile's place);
 // then the tile's keys and values in their in-tile sorted order.
@@ -235,13 +240,12 @@ __host__ __device__ __forceinline__ size_t sort_tile_bytes(size_t key_bytes)
 
 __host__ __device__ __forceinline__ size_t sort_region0_bytes(size_t key_bytes, int nb)
 {
-    const size_t masks = sizeof(uint32_t) * (size_t)(kSortThreads / 32) * (size_t)nb;
-    const size_t tile = sort_tile_bytes(key_bytes) + 64;
+    const size_t masks = sizeof(uint32_t) * (size_t)(kDownThreads / 32) * (size_t)nb;
+    const size_t tile = sort_tile_bytes(key_bytes) + 128;   // + the warp sums (kDownThreads / 32 + 1 words)
     const size_t r = masks > tile ? masks : tile;
     return (r + 15) & ~size_t(15);
 }
 
-constexpr int kDownsweepBlocks = 4;   // resident blocks per SM the ranking kernel's registers are sized for
 
 // Where every tile and group in use lies, one thread per tile (the segment of
 // a tile is a binary search over the segments' first tiles).
@@ -424,12 +428,37 @@ __global__ void __launch_bounds__(kSetupThreads) sort_scan_skips(SortArgs a, Sor
     if (threadIdx.x == 0) sc.skippre[S] = tot;
 }
 
+// A tile's items as the ranking kernel holds them: thread x holds elements
+// warp * (kDownItems * 32) + r * 32 + lane (r < kDownItems).
 template <typename K>
-__global__ void __launch_bounds__(kSortThreads, kDownsweepBlocks) sort_downsweep(SortArgs a, SortScratch sc, int pass)
+__device__ __forceinline__ void load_tile_items(const K* src_k, const uint32_t* src_v, const TileLoc& tl, K (&k)[kDownItems],
+                                                uint32_t (&v)[kDownItems])
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int r = 0; r < kDownItems; ++r) {
+        const int e = warp * (kDownItems * 32) + r * 32 + lane;
+        k[r] = 0;
+        v[r] = 0;
+        if (e < tl.len) {
+            const int64_t idx = tl.start + e;
+            k[r] = src_k[idx];
+            v[r] = src_v ? src_v[idx] : (uint32_t)idx;
+        }
+    }
+}
+
+// The ranking pass.  Persistent blocks walk the tiles (tile, tile + grid,
+// ...); while a tile is ranked and scattered, the next tile's items are
+// already requested (its descriptor one tile earlier still), so the load
+// latency hides behind the work.
+template <typename K>
+__global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep(SortArgs a, SortScratch sc, int pass)
 {
     PassCtx c = pass_ctx(a, pass);
-    const int64_t tile = blockIdx.x;
-    if (!c.active || tile >= sc.seg_tile0[a.num_seg]) return;
+    const int64_t ntiles = sc.seg_tile0[a.num_seg];
+    int64_t tile = blockIdx.x;
+    if (!c.active || tile >= ntiles) return;
     const K* src_k;
     const uint32_t* src_v;
     K* dst_k;
@@ -440,7 +469,7 @@ __global__ void __launch_bounds__(kSortThreads, kDownsweepBlocks) sort_downsweep
     else if (c.dst_out) { src_k = static_cast<const K*>(a.keys_tmp); src_v = a.vals_tmp; }
     else { src_k = static_cast<const K*>(a.keys_out); src_v = a.vals_out; }
 
-    constexpr int kWarps = kSortThreads / 32;
+    constexpr int kWarps = kDownThreads / 32;
     const int nb = 1 << a.D;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // region 0: while ranking, per-warp lane masks of each digit; then the
@@ -452,141 +481,161 @@ __global__ void __launch_bounds__(kSortThreads, kDownsweepBlocks) sort_downsweep
     uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem_raw + sort_tile_bytes(sizeof(K)));   // [kWarps + 1]
     uint32_t* tstart = reinterpret_cast<uint32_t*>(region1);   // [nb]
     uint32_t* gbase = tstart + nb;                // [nb]
-    // per-warp digit counters: at most 32 * kSortItems per warp, so 16 bits
+    // per-warp digit counters: at most 32 * kDownItems per warp, so 16 bits
     uint16_t* wcnt = reinterpret_cast<uint16_t*>(gbase + nb);   // [kWarps][nb]
-
-    for (int i = threadIdx.x; i < kWarps * nb / 2; i += kSortThreads) reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
-    for (int i = threadIdx.x; i < kWarps * nb; i += kSortThreads) wmask[i] = 0u;
-    const TileLoc tl = locate_tile(sc, tile);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int shift = pass * a.D;
     const uint64_t sub = (c.src_in && a.key_sub) ? *a.key_sub : 0ull;
     const uint32_t lt = lanemask_lt();
-    // this thread's digits d0 .. d0+3: where they go (segment start + digit
-    // base + group offset + tile offset) is requested now, so the loads'
-    // latency passes behind the ranking
-    const int per = (nb + kSortThreads - 1) / kSortThreads;   // at most 4 (digits of at most 10 bits)
+    const int per = (nb + kDownThreads - 1) / kDownThreads;   // at most 4 (digits of at most 10 bits)
     const int d0 = threadIdx.x * per;
-    const int64_t grp = tl.grp;
-    uint32_t gb_[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        gb_[q] = 0u;
-        if (q < per && d0 + q < nb)
-            gb_[q] = sc.gsum[grp * nb + d0 + q] + (uint32_t)sc.counts[tile * nb + d0 + q];
-    }
     // the last pass of the layer sort puts skipped ids behind all valid ones
     const bool relocate = a.tables && c.last;
-    uint32_t seg_base = (uint32_t)sc.seg_lo[tl.s];
-    uint32_t skip_base = 0, valid_in_seg = 0, skipd = 0xFFFFFFFFu;
-    if (relocate) {
-        skipd = (uint32_t)(a.skip_key >> shift) & (uint32_t)(nb - 1);
-        const uint32_t pre = sc.skippre[tl.s];
-        valid_in_seg = (uint32_t)sc.seg_len[tl.s] - sc.skipcnt[tl.s];
-        skip_base = (uint32_t)c.n - sc.skippre[a.num_seg] + pre;
-        seg_base -= pre;
-    }
+    const uint32_t skipd = relocate ? (uint32_t)(a.skip_key >> shift) & (uint32_t)(nb - 1) : 0xFFFFFFFFu;
 
-    K k[kSortItems];
-    uint32_t v[kSortItems];
-    uint32_t dg[kSortItems];
-    uint32_t rk[kSortItems];
-#pragma unroll
-    for (int r = 0; r < kSortItems; ++r) {
-        const int e = warp * (kSortItems * 32) + r * 32 + lane;
-        dg[r] = (uint32_t)nb;
-        k[r] = 0;
-        v[r] = 0;
-        if (e < tl.len) {
-            const int64_t idx = tl.start + e;
-            k[r] = src_k[idx];
-            if (c.src_in) k[r] = first_pass_key<K>(a, k[r], tl.s, sub);
-            v[r] = src_v ? src_v[idx] : (uint32_t)idx;
-            dg[r] = (uint32_t)((k[r] >> shift) & (K)(nb - 1));
-        }
-    }
-    __syncthreads();   // the counters and masks are cleared
-    // stable rank of each item among the warp's items of its digit: the lanes
-    // of one step that share a digit find each other through an atomic OR of
-    // their lane bits into the digit's mask; the lowest of them advances the
-    // digit's counter and clears the mask
-    uint32_t* mymask = wmask + warp * nb;
-    uint16_t* mycnt = wcnt + warp * nb;
-#pragma unroll
-    for (int r = 0; r < kSortItems; ++r) {
-        const uint32_t d = dg[r];
-        const bool in = d < (uint32_t)nb;
-        if (in) atomicOr(mymask + d, 1u << lane);
-        __syncwarp();
-        uint32_t peers = 0, base = 0;
-        if (in) {
-            peers = mymask[d];
-            base = mycnt[d];
-        }
-        __syncwarp();
-        if (in && lane == __ffs(peers) - 1) {
-            mycnt[d] = (uint16_t)(base + (uint32_t)__popc(peers));
-            mymask[d] = 0u;
-        }
-        rk[r] = base + (uint32_t)__popc(peers & lt);
-        __syncwarp();
-    }
-    __syncthreads();
-    // per digit: exclusive prefix over warps and the tile total
-    for (int d = threadIdx.x; d < nb; d += kSortThreads) {
-        uint32_t sum = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            uint32_t cnt = wcnt[w * nb + d];
-            wcnt[w * nb + d] = (uint16_t)sum;
-            sum += cnt;
-        }
-        tstart[d] = sum;
-    }
-    __syncthreads();
-    // exclusive scan over digits: tile-local starts; global bases from the scans
-    {
-        uint32_t st = 0;
-        uint32_t lt_[4];
+    TileLoc tl = locate_tile(sc, tile);
+    K kr[kDownItems];
+    uint32_t vr[kDownItems];
+    load_tile_items<K>(src_k, src_v, tl, kr, vr);
+    int64_t next = tile + gridDim.x;
+    TileLoc tn = next < ntiles ? locate_tile(sc, next) : tl;
+    for (;;) {
+        // where this tile's digits go (segment start + digit base + group
+        // offset + tile offset), requested now and used after the ranking
+        uint32_t gb_[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            lt_[q] = (q < per && d0 + q < nb) ? tstart[d0 + q] : 0u;
-            st += lt_[q];
+            gb_[q] = 0u;
+            if (q < per && d0 + q < nb)
+                gb_[q] = sc.gsum[(int64_t)tl.grp * nb + d0 + q] + (uint32_t)sc.counts[tile * nb + d0 + q];
         }
-        uint32_t ext = block_exclusive_sum<kSortThreads>(st, wbuf, nullptr);
+        uint32_t seg_base = (uint32_t)sc.seg_lo[tl.s];
+        uint32_t skip_base = 0, valid_in_seg = 0;
+        if (relocate) {
+            const uint32_t pre = sc.skippre[tl.s];
+            valid_in_seg = (uint32_t)sc.seg_len[tl.s] - sc.skipcnt[tl.s];
+            skip_base = (uint32_t)c.n - sc.skippre[a.num_seg] + pre;
+            seg_base -= pre;
+        }
+        // the next tile's items, and the descriptor of the one after it
+        K kn[kDownItems];
+        uint32_t vn[kDownItems];
+        const int64_t after = next + gridDim.x;
+        TileLoc ta = tn;
+        if (next < ntiles) {
+            load_tile_items<K>(src_k, src_v, tn, kn, vn);
+            if (after < ntiles) ta = locate_tile(sc, after);
+        }
+
+        for (int i = threadIdx.x; i < kWarps * nb / 2; i += kDownThreads) reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
+        for (int i = threadIdx.x; i < kWarps * nb; i += kDownThreads) wmask[i] = 0u;
+        K k[kDownItems];
+        uint32_t dg[kDownItems];
+        uint32_t rk[kDownItems];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int d = d0 + q;
-            if (q < per && d < nb) {
-                tstart[d] = ext;
-                gbase[d] = (uint32_t)d == skipd ? skip_base + (gb_[q] - valid_in_seg) : seg_base + gb_[q];
+        for (int r = 0; r < kDownItems; ++r) {
+            const int e = warp * (kDownItems * 32) + r * 32 + lane;
+            k[r] = kr[r];
+            dg[r] = (uint32_t)nb;
+            if (e < tl.len) {
+                if (c.src_in) k[r] = first_pass_key<K>(a, k[r], tl.s, sub);
+                dg[r] = (uint32_t)((k[r] >> shift) & (K)(nb - 1));
             }
-            ext += lt_[q];
         }
-    }
-    __syncthreads();
+        __syncthreads();   // the counters and masks are cleared
+        // stable rank of each item among the warp's items of its digit: the lanes
+        // of one step that share a digit find each other through an atomic OR of
+        // their lane bits into the digit's mask; the lowest of them advances the
+        // digit's counter and clears the mask
+        uint32_t* mymask = wmask + warp * nb;
+        uint16_t* mycnt = wcnt + warp * nb;
 #pragma unroll
-    for (int r = 0; r < kSortItems; ++r) {
-        if (dg[r] < (uint32_t)nb) {
-            uint32_t lp = tstart[dg[r]] + wcnt[warp * nb + dg[r]] + rk[r];
-            skey[lp] = k[r];
-            sval[lp] = v[r];
+        for (int r = 0; r < kDownItems; ++r) {
+            const uint32_t d = dg[r];
+            const bool in = d < (uint32_t)nb;
+            if (in) atomicOr(mymask + d, 1u << lane);
+            __syncwarp();
+            uint32_t peers = 0, base = 0;
+            if (in) {
+                peers = mymask[d];
+                base = mycnt[d];
+            }
+            __syncwarp();
+            if (in && lane == __ffs(peers) - 1) {
+                mycnt[d] = (uint16_t)(base + (uint32_t)__popc(peers));
+                mymask[d] = 0u;
+            }
+            rk[r] = base + (uint32_t)__popc(peers & lt);
+            __syncwarp();
         }
-    }
-    __syncthreads();
-    const uint32_t rb = a.tables ? a.tables[tl.s].row_base : 0u;
+        __syncthreads();
+        // per digit: exclusive prefix over warps and the tile total
+        for (int d = threadIdx.x; d < nb; d += kDownThreads) {
+            uint32_t sum = 0;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                uint32_t cnt = wcnt[w * nb + d];
+                wcnt[w * nb + d] = (uint16_t)sum;
+                sum += cnt;
+            }
+            tstart[d] = sum;
+        }
+        __syncthreads();
+        // exclusive scan over digits: tile-local starts; global bases from the scans
+        {
+            uint32_t st = 0;
+            uint32_t lt_[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                lt_[q] = (q < per && d0 + q < nb) ? tstart[d0 + q] : 0u;
+                st += lt_[q];
+            }
+            uint32_t ext = block_exclusive_sum<kDownThreads>(st, wbuf, nullptr);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int d = d0 + q;
+                if (q < per && d < nb) {
+                    tstart[d] = ext;
+                    gbase[d] = (uint32_t)d == skipd ? skip_base + (gb_[q] - valid_in_seg) : seg_base + gb_[q];
+                }
+                ext += lt_[q];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < kDownItems; ++r) {
+            if (dg[r] < (uint32_t)nb) {
+                uint32_t lp = tstart[dg[r]] + wcnt[warp * nb + dg[r]] + rk[r];
+                skey[lp] = k[r];
+                sval[lp] = vr[r];
+            }
+        }
+        __syncthreads();
+        const uint32_t rb = a.tables ? a.tables[tl.s].row_base : 0u;
 #pragma unroll 4
-    for (int r = 0; r < kSortItems; ++r) {
-        const int p = r * kSortThreads + threadIdx.x;
-        if (p < tl.len) {
-            K kk = skey[p];
-            const uint32_t d = (uint32_t)((kk >> shift) & (K)(nb - 1));
-            const int64_t o = (int64_t)gbase[d] + (p - (int64_t)tstart[d]);
-            // the layer sort's last pass writes global ids again
-            if (relocate) kk = d == skipd ? (K)a.sentinel : (K)(kk + rb);
-            dst_k[o] = kk;
-            dst_v[o] = sval[p];
+        for (int r = 0; r < kDownItems; ++r) {
+            const int p = r * kDownThreads + threadIdx.x;
+            if (p < tl.len) {
+                K kk = skey[p];
+                const uint32_t d = (uint32_t)((kk >> shift) & (K)(nb - 1));
+                const int64_t o = (int64_t)gbase[d] + (p - (int64_t)tstart[d]);
+                // the layer sort's last pass writes global ids again
+                if (relocate) kk = d == skipd ? (K)a.sentinel : (K)(kk + rb);
+                dst_k[o] = kk;
+                dst_v[o] = sval[p];
+            }
+        }
+        if (next >= ntiles) break;
+        __syncthreads();   // the shared arrays are reused by the next tile
+        tile = next;
+        next = after;
+        tl = tn;
+        tn = ta;
+#pragma unroll
+        for (int r = 0; r < kDownItems; ++r) {
+            kr[r] = kn[r];
+            vr[r] = vn[r];
         }
     }
 }
@@ -681,10 +730,15 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
     const int64_t groups = tiles / kSortGroupTiles + a.num_seg;
     const int nb = 1 << plan.digit_bits;
     const size_t smem = sort_region0_bytes(sizeof(K), nb) + sizeof(uint32_t) * 2 * (size_t)nb +
-                        sizeof(uint16_t) * (size_t)(kSortThreads / 32) * nb;
+                        sizeof(uint16_t) * (size_t)(kDownThreads / 32) * nb;
     if (cudaFuncSetAttribute(sort_downsweep<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
         cudaFuncSetAttribute(sort_downsweep<K>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
         return -1;
+    int dev = 0, sms = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t resident = (int64_t)sms * kDownsweepBlocks;
+    const unsigned ranking_blocks = (unsigned)(tiles < resident ? tiles : resident);
     sort_setup<<<1, kSetupThreads, 0, st>>>(a, sc);
     const unsigned tile_blocks = (unsigned)((tiles + 255) / 256);
     sort_tiles<<<tile_blocks, 256, 0, st>>>(a, sc, tiles);
@@ -698,7 +752,7 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
             sort_scan_skips<<<1, kSetupThreads, 0, st>>>(a, sc, p);
             ++launched;
         }
-        sort_downsweep<K><<<(unsigned)tiles, kSortThreads, smem, st>>>(a, sc, p);
+        sort_downsweep<K><<<ranking_blocks, kDownThreads, smem, st>>>(a, sc, p);
         ++launched;
     }
     if (cudaGetLastError() != cudaSuccess) return -1;

@@ -97,7 +97,9 @@ __host__ __device__ __forceinline__ int64_t warp_words(int64_t c) { return (5 * 
 __device__ __forceinline__ float4 entry_term(const float* gcol, int64_t ld, uint32_t b, uint32_t tB, float f)
 {
     const float4 g = __ldg(reinterpret_cast<const float4*>(gcol + (int64_t)(b - tB) * ld));
-    return make_float4(__fmul_rn(g.x, f), __fmul_rn(g.y, f), __fmul_rn(g.z, f), __fmul_rn(g.w, f));
+    const float2 ff = make_float2(f, f);
+    const float2 lo = mul2(make_float2(g.x, g.y), ff), hi = mul2(make_float2(g.z, g.w), ff);
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 __device__ __forceinline__ float entry_factor(const ReduceArgs& a, const uint16_t* epos, int e, uint32_t b, bool mean)
@@ -225,9 +227,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
     // lanes per row for this chunk: enough for the widest table among its runs
     // (the chunk's lookups are sorted, so its tables form one range, usually one table)
     int Lg = 1;
+    int t_one = -1;   // the chunk's table when all its lookups belong to one
     {
         const int t_first = min((int)(ebag[0] / (uint32_t)a.batch), a.num_tables - 1);
         const int t_last = min((int)(ebag[E - 1] / (uint32_t)a.batch), a.num_tables - 1);
+        if (t_first == t_last) t_one = t_first;
         int maxdim = 4;
         for (int t = t_first; t <= t_last; ++t) maxdim = max(maxdim, a.tables[t].dim);
         while (4 * Lg < maxdim) Lg <<= 1;
@@ -308,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
         if (key >= limit) continue;
         const bool before = r == 0 && first_before;
         const bool after = r == R - 1 && last_after;
-        const int t = (int)(ebag[e0] / (uint32_t)a.batch);
+        const int t = t_one >= 0 ? t_one : (int)(ebag[e0] / (uint32_t)a.batch);
         if (t >= a.num_tables) continue;   // only ids left by a forward whose offsets were flagged
         const TableDev& tb = a.tables[t];
         const uint32_t tB = (uint32_t)t * (uint32_t)a.batch;
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
             wv = load_update_w4(tb, elem);
             av = load_state4(tb, row, elem);
         }
-        float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 sa = make_float2(0.f, 0.f), sb = sa, ca = sa, cb = sa;
         if (colok) {
             const float* gcol = a.grad + tb.doff + 4 * li;
             int q = e0;
@@ -334,23 +338,18 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
                 const float4 ta = entry_term(gcol, a.ld, ba, tB, entry_factor(a, epos, q, ba, mean));
                 const float4 tb4 = entry_term(gcol, a.ld, bb, tB, entry_factor(a, epos, q + 1, bb, mean));
                 // the pair is added in plain fp32, then compensated into the run sum
-                kahan_add(s[0], c[0], __fadd_rn(ta.x, tb4.x));
-                kahan_add(s[1], c[1], __fadd_rn(ta.y, tb4.y));
-                kahan_add(s[2], c[2], __fadd_rn(ta.z, tb4.z));
-                kahan_add(s[3], c[3], __fadd_rn(ta.w, tb4.w));
+                kahan_add2(sa, ca, add2(make_float2(ta.x, ta.y), make_float2(tb4.x, tb4.y)));
+                kahan_add2(sb, cb, add2(make_float2(ta.z, ta.w), make_float2(tb4.z, tb4.w)));
             }
             if (q < e1) {
                 const uint32_t ba = ebag[q];
                 const float4 ta = entry_term(gcol, a.ld, ba, tB, entry_factor(a, epos, q, ba, mean));
-                kahan_add(s[0], c[0], ta.x);
-                kahan_add(s[1], c[1], ta.y);
-                kahan_add(s[2], c[2], ta.z);
-                kahan_add(s[3], c[3], ta.w);
+                kahan_add2(sa, ca, make_float2(ta.x, ta.y));
+                kahan_add2(sb, cb, make_float2(ta.z, ta.w));
             }
         }
-        float gs[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) gs[k] = __fsub_rn(s[k], c[k]);
+        const float2 ra = sub2(sa, ca), rb = sub2(sb, cb);
+        float gs[4] = {ra.x, ra.y, rb.x, rb.y};
         if (before || after) {
             if (colok) {
                 float* sp = slot_ptr(a.slots, chunk, before ? kSlotHead : kSlotTail);

@@ -80,6 +80,7 @@ struct SortScratch {
     uint32_t* gsum;         // [groups][nb] per-group sums, then group offsets + segment digit bases
     int4* tile_desc;        // [tiles] first position, length, segment, group of each tile in use
     int4* grp_desc;         // [groups] first tile, tiles, segment of each group in use
+    uint32_t* segtot;       // [S][nb] the segments' digit totals, then their exclusive digit bases
 };
 
 // The per-pass context every kernel derives the same way from the device or
@@ -348,59 +349,90 @@ __global__ void __launch_bounds__(kSortThreads) sort_scan_groups(SortArgs a, Sor
     }
 }
 
-// Per segment: each group's sum becomes the group's exclusive offset within
-// the segment plus the segment's exclusive digit base; on the last pass of
-// the layer sort the segment's count of skipped ids (the all-ones top digit)
-// is recorded.
-__global__ void __launch_bounds__(kSortThreads) sort_scan_segments(SortArgs a, SortScratch sc, int pass)
+// The segments' scans, in three steps that each run in parallel:
+//  1. per segment and slice of 32 digits: each group's sum becomes its
+//     exclusive offset within the segment (8 warps take consecutive runs of
+//     the segment's groups, lane = digit), and the segment's digit totals go
+//     to segtot;
+//  2. per segment: the totals become the segment's exclusive digit bases; on
+//     the last pass of the layer sort the segment's count of skipped ids (the
+//     all-ones top digit) is recorded;
+//  3. per group: the segment's digit bases are added to the group offsets.
+constexpr int kScanWarps = 8;
+
+__global__ void __launch_bounds__(kScanWarps * 32) sort_scan_segments(SortArgs a, SortScratch sc, int pass)
 {
     PassCtx c = pass_ctx(a, pass);
     const int s = blockIdx.x;
     if (!c.active || s >= a.num_seg) return;
-    __shared__ uint32_t tot[1 << kMaxDigitBits];
-    __shared__ uint32_t wbuf[kSortThreads / 32 + 1];
     const int nb = 1 << a.D;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int d = blockIdx.y * 32 + lane;
+    __shared__ uint32_t wsum[kScanWarps][32];
     const int64_t g0 = sc.seg_grp0[s], g1 = sc.seg_grp0[s + 1];
+    const int64_t per = (g1 - g0 + kScanWarps - 1) / kScanWarps;
+    const int64_t ga = g0 + warp * per, gb = ga + per < g1 ? ga + per : g1;
     constexpr int kB = 8;   // group sums loaded per batch
-    for (int d = threadIdx.x; d < nb; d += kSortThreads) {
-        uint32_t run = 0;
-        for (int64_t g = g0; g < g1; g += kB) {
+    uint32_t run = 0;
+    if (d < nb) {
+        for (int64_t g = ga; g < gb; g += kB) {
             uint32_t v[kB];
 #pragma unroll
-            for (int q = 0; q < kB; ++q) v[q] = g + q < g1 ? sc.gsum[(g + q) * nb + d] : 0u;
+            for (int q = 0; q < kB; ++q) v[q] = g + q < gb ? sc.gsum[(g + q) * nb + d] : 0u;
+#pragma unroll
+            for (int q = 0; q < kB; ++q) run += v[q];
+        }
+    }
+    wsum[warp][lane] = run;
+    __syncthreads();
+    uint32_t off = 0;
+    for (int w = 0; w < warp; ++w) off += wsum[w][lane];
+    if (d < nb) {
+        for (int64_t g = ga; g < gb; g += kB) {
+            uint32_t v[kB];
+#pragma unroll
+            for (int q = 0; q < kB; ++q) v[q] = g + q < gb ? sc.gsum[(g + q) * nb + d] : 0u;
 #pragma unroll
             for (int q = 0; q < kB; ++q) {
-                if (g + q < g1) sc.gsum[(g + q) * nb + d] = run;
-                run += v[q];
+                if (g + q < gb) sc.gsum[(g + q) * nb + d] = off;
+                off += v[q];
             }
         }
-        tot[d] = run;
+        if (warp == kScanWarps - 1) sc.segtot[(int64_t)s * nb + d] = off;
     }
-    __syncthreads();
-    // exclusive scan of the segment's digit totals (a thread takes 4 consecutive digits)
-    uint32_t lt[4], sum = 0;
-    const int d0 = threadIdx.x * 4;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        lt[q] = d0 + q < nb ? tot[d0 + q] : 0u;
-        sum += lt[q];
-    }
-    uint32_t ex = block_exclusive_sum<kSortThreads>(sum, wbuf, nullptr);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (d0 + q < nb) tot[d0 + q] = ex;
-        ex += lt[q];
-    }
-    __syncthreads();
-    for (int d = threadIdx.x; d < nb; d += kSortThreads) {
-        const uint32_t base = tot[d];
-        for (int64_t g = g0; g < g1; ++g) sc.gsum[g * nb + d] += base;
-    }
-    if (a.tables && c.last && threadIdx.x == 0) {
+}
+
+__global__ void __launch_bounds__(1024) sort_seg_bases(SortArgs a, SortScratch sc, int pass)
+{
+    PassCtx c = pass_ctx(a, pass);
+    const int s = blockIdx.x;
+    if (!c.active || s >= a.num_seg) return;
+    __shared__ uint32_t wbuf[1024 / 32 + 1];
+    __shared__ uint32_t skip_base;
+    const int nb = 1 << a.D;
+    const int d = threadIdx.x;
+    uint32_t* tot = sc.segtot + (int64_t)s * nb;
+    const uint32_t v = d < nb ? tot[d] : 0u;
+    const uint32_t ex = block_exclusive_sum<1024>(v, wbuf, nullptr);
+    const uint32_t skipd = (uint32_t)(a.skip_key >> (pass * a.D)) & (uint32_t)(nb - 1);
+    if (d < nb) {
+        tot[d] = ex;
         // skipped ids carry the largest digit, so everything before its base is valid
-        const uint32_t skipd = (uint32_t)(a.skip_key >> (pass * a.D)) & (uint32_t)(nb - 1);
-        sc.skipcnt[s] = (uint32_t)sc.seg_len[s] - tot[skipd];
+        if (a.tables && c.last && (uint32_t)d == skipd) skip_base = ex;
     }
+    __syncthreads();
+    if (a.tables && c.last && threadIdx.x == 0) sc.skipcnt[s] = (uint32_t)sc.seg_len[s] - skip_base;
+}
+
+__global__ void __launch_bounds__(256) sort_add_bases(SortArgs a, SortScratch sc, int pass)
+{
+    PassCtx c = pass_ctx(a, pass);
+    const int64_t grp = blockIdx.x;
+    if (!c.active || grp >= sc.seg_grp0[a.num_seg]) return;
+    const int nb = 1 << a.D;
+    const int s = sc.grp_desc[grp].z;
+    const uint32_t* base = sc.segtot + (int64_t)s * nb;
+    for (int d = threadIdx.x; d < nb; d += 256) sc.gsum[grp * nb + d] += base[d];
 }
 
 // Exclusive prefix of the skipped ids over segments (last pass of the layer sort).
@@ -642,7 +674,7 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
 
 // Byte offsets of the scratch arrays inside one region (host and device agree).
 struct ScratchLayout {
-    size_t seg_lo, seg_len, seg_tile0, seg_grp0, skipcnt, skippre, counts, gsum, tile_desc, grp_desc, total;
+    size_t seg_lo, seg_len, seg_tile0, seg_grp0, skipcnt, skippre, counts, gsum, tile_desc, grp_desc, segtot, total;
 };
 
 ScratchLayout scratch_layout(const SortPlan& p)
@@ -666,6 +698,7 @@ ScratchLayout scratch_layout(const SortPlan& p)
     l.gsum = take(4 * nb * (size_t)p.groups_max);
     l.tile_desc = take(16 * (size_t)p.tiles_max);
     l.grp_desc = take(16 * (size_t)p.groups_max);
+    l.segtot = take(4 * nb * S);
     l.total = off;
     return l;
 }
@@ -725,6 +758,7 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
     sc.gsum = reinterpret_cast<uint32_t*>(base + l.gsum);
     sc.tile_desc = reinterpret_cast<int4*>(base + l.tile_desc);
     sc.grp_desc = reinterpret_cast<int4*>(base + l.grp_desc);
+    sc.segtot = reinterpret_cast<uint32_t*>(base + l.segtot);
 
     const int64_t tiles = (a.n_host + kSortTile - 1) / kSortTile + a.num_seg;
     const int64_t groups = tiles / kSortGroupTiles + a.num_seg;
@@ -746,8 +780,10 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
     for (int p = 0; p < plan.passes_max; ++p) {
         sort_upsweep<K><<<(unsigned)tiles, kSortThreads, 0, st>>>(a, sc, p);
         sort_scan_groups<<<(unsigned)groups, kSortThreads, 0, st>>>(a, sc, p);
-        sort_scan_segments<<<(unsigned)a.num_seg, kSortThreads, 0, st>>>(a, sc, p);
-        launched += 3;
+        sort_scan_segments<<<dim3((unsigned)a.num_seg, (unsigned)((nb + 31) / 32)), kScanWarps * 32, 0, st>>>(a, sc, p);
+        sort_seg_bases<<<(unsigned)a.num_seg, 1024, 0, st>>>(a, sc, p);
+        sort_add_bases<<<(unsigned)groups, 256, 0, st>>>(a, sc, p);
+        launched += 5;
         if (a.tables) {
             sort_scan_skips<<<1, kSetupThreads, 0, st>>>(a, sc, p);
             ++launched;

@@ -231,9 +231,15 @@ constexpr int kDownThreads = 256;      // ranking block: 8 warps ...
 constexpr int kDownItems = kSortTile / kDownThreads;   // ... of 12 items each per tile
 static_assert(kDownItems * kDownThreads == kSortTile, "the ranking block covers one tile");
 
-// Bytes of the ranking kernel's first shared region: the per-warp digit masks
-// while ranking; then the block scans' warp sums (behind the tile's place);
-// then the tile's keys and values in their in-tile sorted order.
+// Shared memory of the ranking kernel: the per-warp digit masks (all zero
+// between ranking steps), the tile's keys and values in their in-tile sorted
+// order followed by the block scans' warp sums, then per-digit starts, bases
+// and per-warp counters.
+__host__ __device__ __forceinline__ size_t sort_masks_bytes(int nb)
+{
+    return sizeof(uint32_t) * (size_t)(kDownThreads / 32) * (size_t)nb;
+}
+
 __host__ __device__ __forceinline__ size_t sort_tile_bytes(size_t key_bytes)
 {
     return ((size_t)kSortTile * (key_bytes + sizeof(uint32_t)) + 15) & ~size_t(15);
@@ -241,10 +247,7 @@ __host__ __device__ __forceinline__ size_t sort_tile_bytes(size_t key_bytes)
 
 __host__ __device__ __forceinline__ size_t sort_region0_bytes(size_t key_bytes, int nb)
 {
-    const size_t masks = sizeof(uint32_t) * (size_t)(kDownThreads / 32) * (size_t)nb;
-    const size_t tile = sort_tile_bytes(key_bytes) + 128;   // + the warp sums (kDownThreads / 32 + 1 words)
-    const size_t r = masks > tile ? masks : tile;
-    return (r + 15) & ~size_t(15);
+    return sort_masks_bytes(nb) + sort_tile_bytes(key_bytes) + 128;   // + the warp sums (kDownThreads / 32 + 1 words)
 }
 
 
@@ -504,13 +507,14 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
     constexpr int kWarps = kDownThreads / 32;
     const int nb = 1 << a.D;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    // region 0: while ranking, per-warp lane masks of each digit; then the
-    // tile's keys and values in their in-tile sorted order
+    // the per-warp lane masks of each digit (zero between ranking steps), then
+    // the tile's keys and values in their in-tile sorted order
     uint32_t* wmask = reinterpret_cast<uint32_t*>(smem_raw);   // [kWarps][nb]
-    K* skey = reinterpret_cast<K*>(smem_raw);
+    unsigned char* stage = smem_raw + sort_masks_bytes(nb);
+    K* skey = reinterpret_cast<K*>(stage);
     uint32_t* sval = reinterpret_cast<uint32_t*>(skey + kSortTile);
     unsigned char* region1 = smem_raw + sort_region0_bytes(sizeof(K), nb);
-    uint32_t* wbuf = reinterpret_cast<uint32_t*>(smem_raw + sort_tile_bytes(sizeof(K)));   // [kWarps + 1]
+    uint32_t* wbuf = reinterpret_cast<uint32_t*>(stage + sort_tile_bytes(sizeof(K)));   // [kWarps + 1]
     uint32_t* tstart = reinterpret_cast<uint32_t*>(region1);   // [nb]
     uint32_t* gbase = tstart + nb;                // [nb]
     // per-warp digit counters: at most 32 * kDownItems per warp, so 16 bits
@@ -526,6 +530,8 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
     const bool relocate = a.tables && c.last;
     const uint32_t skipd = relocate ? (uint32_t)(a.skip_key >> shift) & (uint32_t)(nb - 1) : 0xFFFFFFFFu;
 
+    // the masks start at zero; each ranking step's lowest lane clears what it set
+    for (int i = threadIdx.x; i < kWarps * nb; i += kDownThreads) wmask[i] = 0u;
     TileLoc tl = locate_tile(sc, tile);
     K kr[kDownItems];
     uint32_t vr[kDownItems];
@@ -561,7 +567,6 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
         }
 
         for (int i = threadIdx.x; i < kWarps * nb / 2; i += kDownThreads) reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
-        for (int i = threadIdx.x; i < kWarps * nb; i += kDownThreads) wmask[i] = 0u;
         K k[kDownItems];
         uint32_t dg[kDownItems];
         uint32_t rk[kDownItems];
@@ -575,7 +580,7 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
                 dg[r] = (uint32_t)((k[r] >> shift) & (K)(nb - 1));
             }
         }
-        __syncthreads();   // the counters and masks are cleared
+        __syncthreads();   // the counters are cleared
         // stable rank of each item among the warp's items of its digit: the lanes
         // of one step that share a digit find each other through an atomic OR of
         // their lane bits into the digit's mask; the lowest of them advances the

@@ -276,7 +276,7 @@ __global__ void sort_tiles(SortArgs a, SortScratch sc, int64_t tiles_grid)
 struct TileLoc {
     int s;
     int grp;
-    int64_t start;
+    int start;   // positions fit in 32 bits (fewer than 2^31 elements)
     int len;
 };
 
@@ -476,7 +476,7 @@ __device__ __forceinline__ void load_tile_items(const K* src_k, const uint32_t* 
         k[r] = 0;
         v[r] = 0;
         if (e < tl.len) {
-            const int64_t idx = tl.start + e;
+            const uint32_t idx = (uint32_t)(tl.start + e);
             k[r] = src_k[idx];
             v[r] = src_v ? src_v[idx] : (uint32_t)idx;
         }
@@ -511,8 +511,10 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
     // the tile's keys and values in their in-tile sorted order
     uint32_t* wmask = reinterpret_cast<uint32_t*>(smem_raw);   // [kWarps][nb]
     unsigned char* stage = smem_raw + sort_masks_bytes(nb);
+    // 32-bit keys travel with their values as one 8-byte pair
     K* skey = reinterpret_cast<K*>(stage);
     uint32_t* sval = reinterpret_cast<uint32_t*>(skey + kSortTile);
+    uint2* spair = reinterpret_cast<uint2*>(stage);
     unsigned char* region1 = smem_raw + sort_region0_bytes(sizeof(K), nb);
     uint32_t* wbuf = reinterpret_cast<uint32_t*>(stage + sort_tile_bytes(sizeof(K)));   // [kWarps + 1]
     uint32_t* tstart = reinterpret_cast<uint32_t*>(region1);   // [nb]
@@ -634,7 +636,8 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
                 const int d = d0 + q;
                 if (q < per && d < nb) {
                     tstart[d] = ext;
-                    gbase[d] = (uint32_t)d == skipd ? skip_base + (gb_[q] - valid_in_seg) : seg_base + gb_[q];
+                    // where the digit's run starts globally, less its start in the tile
+                    gbase[d] = ((uint32_t)d == skipd ? skip_base + (gb_[q] - valid_in_seg) : seg_base + gb_[q]) - ext;
                 }
                 ext += lt_[q];
             }
@@ -644,8 +647,12 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
         for (int r = 0; r < kDownItems; ++r) {
             if (dg[r] < (uint32_t)nb) {
                 uint32_t lp = tstart[dg[r]] + wcnt[warp * nb + dg[r]] + rk[r];
-                skey[lp] = k[r];
-                sval[lp] = vr[r];
+                if constexpr (sizeof(K) == 4) {
+                    spair[lp] = make_uint2((uint32_t)k[r], vr[r]);
+                } else {
+                    skey[lp] = k[r];
+                    sval[lp] = vr[r];
+                }
             }
         }
         __syncthreads();
@@ -654,13 +661,23 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
         for (int r = 0; r < kDownItems; ++r) {
             const int p = r * kDownThreads + threadIdx.x;
             if (p < tl.len) {
-                K kk = skey[p];
+                K kk;
+                uint32_t vv;
+                if constexpr (sizeof(K) == 4) {
+                    const uint2 pr = spair[p];
+                    kk = (K)pr.x;
+                    vv = pr.y;
+                } else {
+                    kk = skey[p];
+                    vv = sval[p];
+                }
                 const uint32_t d = (uint32_t)((kk >> shift) & (K)(nb - 1));
-                const int64_t o = (int64_t)gbase[d] + (p - (int64_t)tstart[d]);
+                // gbase holds (global start - tile start) per digit; positions fit in 32 bits
+                const uint32_t o = gbase[d] + (uint32_t)p;
                 // the layer sort's last pass writes global ids again
                 if (relocate) kk = d == skipd ? (K)a.sentinel : (K)(kk + rb);
                 dst_k[o] = kk;
-                dst_v[o] = sval[p];
+                dst_v[o] = vv;
             }
         }
         if (next >= ntiles) break;

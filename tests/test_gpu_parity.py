@@ -265,6 +265,45 @@ def test_wrong_table_id_is_reported():
         layer.close()
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_table_segments_with_skipped_ids_over_several_passes(variant):
+    """The dedup sorts each table's lookups on their table-local row id.  Tables
+    of very different sizes (one-pass and multi-pass local ids; 2^20 - 1 rows,
+    whose largest id would share the top digit of the skipped-id key without
+    one more bit), skipped ids in several tables moved behind every valid id,
+    and an empty first table."""
+    from dlrm_sparse_embedding_gb300 import EMB_ERR_KEY_RANGE
+    tabs = [ci.TableSpec(50, 8), ci.TableSpec((1 << 20) - 1, 4, opt="adagrad"), ci.TableSpec(1023, 16),
+            ci.TableSpec(300_000, 8, pooling="mean"), ci.TableSpec(1024, 4)]
+    B = 3000
+    rng0 = np.random.default_rng(11)
+    lens = rng0.integers(0, 12, size=len(tabs) * B)
+    lens[:B] = 0                      # table 0: no lookups at all
+
+    def keys(rng, t, s, L):
+        k = rng.integers(0, s.rows, L)
+        top = rng.random(L) < 0.2
+        k[top] = s.rows - 1 - rng.integers(0, 2, int(top.sum())).clip(0, s.rows - 1)
+        bad = rng.random(L) < 0.05
+        k[bad] = rng.choice([-1, s.rows, s.rows + 7], size=int(bad.sum()))
+        return k
+
+    w, b, g = _custom(tabs, B, lens, keys, seed=21)
+    check_step(w, b, g, variant, expect_status=EMB_ERR_KEY_RANGE)
+
+
+@pytest.mark.parametrize("variant", ["reduction", "unique_hash"])
+def test_many_small_tables(variant):
+    """1300 tables (more segments than the sort's set-up block has threads),
+    a few bags each, some tables empty."""
+    T, B = 1300, 8
+    tabs = [ci.TableSpec(10 + (t * 37) % 200, 4 * (1 + t % 3)) for t in range(T)]
+    lens = np.random.default_rng(4).integers(0, 4, size=T * B)
+    lens[5 * B:6 * B] = 0
+    w, b, g = _custom(tabs, B, lens, lambda rng, t, s, L: rng.integers(0, s.rows, L), seed=5)
+    check_step(w, b, g, variant, sample_untouched=2)
+
+
 @pytest.mark.parametrize("hot", [1, 7])
 def test_bad_offsets_are_clamped_and_reported(hot):
     """Offsets past nnz or decreasing are clamped on the GPU and reported as a

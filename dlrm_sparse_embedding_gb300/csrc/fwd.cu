@@ -240,7 +240,8 @@ __device__ __forceinline__ void pool_bags(const FwdArgs& a, const TableDev& tb, 
 // at ((r * kThreads) + x) * SLOT bytes (SLOT = 16, or 8 where every table
 // stores 16-bit rows), so a warp's reads of a slot are conflict-free; no lane
 // ever reads another lane's slots.
-constexpr int kRing = 16;   // slots per lane: two batches of eight rows
+constexpr int kRingBatch = 8;             // rows a lane requests at once
+constexpr int kRing = 2 * kRingBatch;     // slots per lane: two batches
 
 // Shared memory of one block's rings: slots of 16 bytes, or 8 in the kernel
 // for layers whose tables all store 16-bit rows.
@@ -304,24 +305,24 @@ __device__ __forceinline__ void pool_bags_ring(const FwdArgs& a, const TableDev&
             // batch b (keys 8b .. 8b+7 of the window) goes to slots 8*(b&1) ..
             auto request = [&](int b) {
 #pragma unroll
-                for (int u = 0; u < kPrefetch; ++u) {
-                    const int q = b * kPrefetch + u;
+                for (int u = 0; u < kRingBatch; ++u) {
+                    const int q = b * kRingBatch + u;
                     const uint32_t kq = __shfl_sync(gmask, kk[q / LR], q % LR, LR);
                     const bool live = q < n && kq != kNoRow && colok;
-                    ring_copy(ring + (uint32_t)((b & 1) * kPrefetch + u) * kSlot,
+                    ring_copy(ring + (uint32_t)((b & 1) * kRingBatch + u) * kSlot,
                               live ? wlane + (uint64_t)kq * rbytes : wlane, F32, live);
                 }
                 ring_commit();
             };
-            const int nb = (n + kPrefetch - 1) / kPrefetch;
+            const int nb = (n + kRingBatch - 1) / kRingBatch;
             request(0);
             for (int b = 0; b < nb; ++b) {
                 if (b + 1 < nb) request(b + 1);
                 else ring_commit();       // an empty group keeps "all but the newest" meaning batch b
                 ring_wait_one();
-                const uint32_t base = ring + (uint32_t)((b & 1) * kPrefetch) * kSlot;
+                const uint32_t base = ring + (uint32_t)((b & 1) * kRingBatch) * kSlot;
 #pragma unroll
-                for (int u = 0; u < kPrefetch; ++u) {
+                for (int u = 0; u < kRingBatch; ++u) {
                     float4 x;
                     if constexpr (F32) {
                         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -571,8 +572,7 @@ int launch_forward(const FwdArgs& a, cudaStream_t st)
     } else {
         auto kernel = a.rows16 ? fwd_pool<kBlocks16, false> : fwd_pool<3, false>;
         const int smem = ring_bytes(a.rows16 ? 8 : 16);
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return -1;
         kernel<<<blocks, kThreads, smem, st>>>(a);
     }

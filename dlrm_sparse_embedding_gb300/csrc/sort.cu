@@ -806,7 +806,7 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
         sort_seg_bases<<<(unsigned)a.num_seg, 1024, 0, st>>>(a, sc, p);
         sort_add_bases<<<(unsigned)groups, 256, 0, st>>>(a, sc, p);
         launched += 5;
-        if (a.tables) {
+        if (a.tables && (a.bits_dev || p == plan.passes_max - 1)) {   // the last pass (known here unless bits are on the device)
             sort_scan_skips<<<1, kSetupThreads, 0, st>>>(a, sc, p);
             ++launched;
         }

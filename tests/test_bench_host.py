@@ -98,7 +98,7 @@ def test_recorded_traffic_only_while_the_kernel_source_is_unchanged(tmp_path):
 
 
 def test_committed_traffic_record_names_the_reduction_sources():
-    with open(os.path.join(bench.ROOT, "profiles", "traffic_dlrm_reduction.json")) as f:
+    with open(os.path.join(bench.ROOT, "profiles", "traffic_multihot_reduction.json")) as f:
         rec = json.load(f)["reduce_update"]
     assert set(rec["sources_sha256"]) == {"dlrm_sparse_embedding_gb300/csrc/update.cu",
                                           "dlrm_sparse_embedding_gb300/csrc/emb_internal.cuh"}

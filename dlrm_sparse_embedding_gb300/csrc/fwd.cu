@@ -100,15 +100,6 @@ __device__ __forceinline__ void sum2_add(float2& s, float2& c, float2 x)
     s = t;
 }
 
-// A lookup's 4 columns of this lane as they travel from memory to the sum:
-// fp32 rows as float4, 16-bit rows as their raw 8 bytes (converted when the
-// row is added), and in the inference forward always as float4 (a cached row
-// comes from the table's fp16 cache).
-template <int DT, bool kInfer>
-struct RowBits {
-    using T = typename std::conditional<DT == EMB_F32 || kInfer, float4, uint2>::type;
-};
-
 __device__ __forceinline__ float4 bits16_to_f32(uint2 r, int dtype)
 {
     if (dtype == EMB_F16) {
@@ -119,118 +110,6 @@ __device__ __forceinline__ float4 bits16_to_f32(uint2 r, int dtype)
     const float2 fa = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r.x));
     const float2 fb = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r.y));
     return make_float4(fa.x, fa.y, fb.x, fb.y);
-}
-
-template <int DT, bool kInfer>
-__device__ __forceinline__ typename RowBits<DT, kInfer>::T fetch_row(const TableDev& tb, const char* wlane, uint32_t kq,
-                                                                      uint32_t rbytes, int li)
-{
-    const char* p = wlane + (uint64_t)kq * rbytes;
-    if constexpr (kInfer) {
-        if (tb.cache_w && (kq & kCacheBit)) return load_cached_row4(tb, kq & ~kCacheBit, li);
-        if constexpr (DT == EMB_F32) return __ldg(reinterpret_cast<const float4*>(p));
-        else return bits16_to_f32(__ldg(reinterpret_cast<const uint2*>(p)), DT);
-    } else {
-        if constexpr (DT == EMB_F32) return __ldg(reinterpret_cast<const float4*>(p));
-        else return __ldg(reinterpret_cast<const uint2*>(p));
-    }
-}
-
-template <int DT, bool kInfer>
-__device__ __forceinline__ float4 row_f32(typename RowBits<DT, kInfer>::T r)
-{
-    if constexpr (DT == EMB_F32 || kInfer) return r;
-    else return bits16_to_f32(r, DT);
-}
-
-template <int DT, bool kInfer>
-__device__ __forceinline__ typename RowBits<DT, kInfer>::T zero_row()
-{
-    if constexpr (DT == EMB_F32 || kInfer) return make_float4(0.f, 0.f, 0.f, 0.f);
-    else return make_uint2(0u, 0u);
-}
-
-// Pools the group's bags one after another (bags of several keys) of a table
-// stored as DT.  Positions fit in 32 bits (fewer than 2^31 lookups).  A bag's
-// keys are taken in windows of WIN (32; 8 or 16 for rows of at most 8
-// columns): lane li loads positions w + li + j*LR (j < KPL), checks them,
-// writes their global ids and bag for the backward, and keeps a 32-bit row
-// code per key (kNoRow for a skipped lookup).  The window's rows are then
-// requested eight per lane at a time (each key's code broadcast from the lane
-// that loaded it) and added in key order as terms of the bag's cascaded
-// compensated sum, two columns per instruction; a skipped key or a position
-// past the bag adds an exact zero, which leaves the sum unchanged.  The
-// result is scaled for mean pooling and stored into the bag's output slice.
-template <int LR, bool kInfer, int DT>
-__device__ __forceinline__ void pool_bags(const FwdArgs& a, const TableDev& tb, const int64_t* kp, int li,
-                                          uint32_t gmask, int64_t j0, int nbg, int my_start, int my_end,
-                                          bool my_tid_ok, bool colok, float* out_col, int64_t bg0)
-{
-    constexpr int KPL = LR >= 4 ? 32 / LR : 8;   // keys each lane loads per window
-    constexpr int WIN = KPL * LR;                // keys per window
-    using Row = typename RowBits<DT, kInfer>::T;
-    const char* wlane = static_cast<const char*>(tb.w) + (DT == EMB_F32 ? 16 : 8) * li;
-    const uint32_t rbytes = (uint32_t)tb.dim * (DT == EMB_F32 ? 4u : 2u);
-    const bool mean = tb.pooling == EMB_POOL_MEAN;
-    for (int k = 0; k < nbg; ++k) {
-        const int s0 = __shfl_sync(gmask, my_start, k, LR);
-        const int e0 = __shfl_sync(gmask, my_end, k, LR);
-        const bool tok = __shfl_sync(gmask, my_tid_ok, k, LR);
-        float2 sa = make_float2(0.f, 0.f), sb = sa, ca = sa, cb = sa;
-        for (int w = s0; w < e0; w += WIN) {
-            uint32_t kk[KPL];
-#pragma unroll
-            for (int j = 0; j < KPL; ++j) {
-                const int p = w + li + j * LR;
-                kk[j] = kNoRow;
-                if (p < e0) {
-                    const int64_t key = __ldg(kp + p);
-                    const bool valid = tok && key >= 0 && key < tb.rows;
-                    if (!kInfer && a.write_ids) {
-                        a.gid_out[p] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
-                        a.bag_out[p] = (uint32_t)(j0 + k);
-                    }
-                    if (!valid && tok && !(kInfer && tb.dynamic)) atomicOr(a.err, ERRBIT_KEY_RANGE);
-                    if (valid) {
-                        kk[j] = (uint32_t)key;
-                        // a cached row travels as its cache slot with kCacheBit set
-                        // (tables with a cache have fewer than 2^31 rows)
-                        if (kInfer && tb.cache_map) {
-                            const int64_t cs = cache_slot_of(tb, key);
-                            if (cs >= 0) kk[j] = kCacheBit | (uint32_t)cs;
-                        }
-                    }
-                }
-            }
-            const int n = e0 - w < WIN ? e0 - w : WIN;
-#pragma unroll
-            for (int b = 0; b < WIN; b += kPrefetch) {
-                if (b >= n) break;
-                Row v[kPrefetch];
-#pragma unroll
-                for (int u = 0; u < kPrefetch; ++u) {
-                    const int q = b + u;
-                    const uint32_t kq = __shfl_sync(gmask, kk[q / LR], q % LR, LR);
-                    v[u] = zero_row<DT, kInfer>();
-                    if (q < n && kq != kNoRow && colok) v[u] = fetch_row<DT, kInfer>(tb, wlane, kq, rbytes, li);
-                }
-#pragma unroll
-                for (int u = 0; u < kPrefetch; ++u) {
-                    const float4 x = row_f32<DT, kInfer>(v[u]);
-                    sum2_add(sa, ca, make_float2(x.x, x.y));
-                    sum2_add(sb, cb, make_float2(x.z, x.w));
-                }
-            }
-        }
-        const float2 ra = add2(sa, ca), rb = add2(sb, cb);
-        float4 r = make_float4(ra.x, ra.y, rb.x, rb.y);
-        const int L = e0 - s0;
-        if (mean && L > 0) {
-            const float fl = (float)L;
-            r = make_float4(__fdiv_rn(r.x, fl), __fdiv_rn(r.y, fl), __fdiv_rn(r.z, fl), __fdiv_rn(r.w, fl));
-        }
-        if (colok) __stcs(reinterpret_cast<float4*>(out_col + (bg0 + k) * a.ld), r);
-    }
 }
 
 // Rows requested ahead through shared memory: each lane copies its 16 bytes
@@ -258,14 +137,33 @@ __device__ __forceinline__ void ring_copy(uint32_t dst, const char* src, bool f3
         asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
 
+// An 8-byte copy into a slot: a cached row's 4 fp16 columns in the inference
+// forward (8-byte aligned whatever the slot size).
+__device__ __forceinline__ void ring_copy8(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ void ring_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void ring_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// pool_bags for the training forward, with the rows of a window's keys
-// travelling through the lane's shared-memory ring: the next batch of eight
-// rows is requested before the current batch is added, so up to sixteen rows
-// per lane are in flight.
-template <int LR, int DT, int SLOT>
+// Pools the group's bags one after another (bags of several keys) of a table
+// stored as DT.  Positions fit in 32 bits (fewer than 2^31 lookups).  A bag's
+// keys are taken in windows of WIN (32; 8 or 16 for rows of at most 8
+// columns): lane li loads positions w + li + j*LR (j < KPL), checks them,
+// writes their global ids and bag for the backward, and keeps a 32-bit row
+// code per key (kNoRow for a skipped lookup).  The window's rows travel
+// through the lanes' shared-memory rings, eight per lane at a time (each
+// key's code broadcast from the lane that loaded it): the next batch is
+// requested before the current batch is added, so up to sixteen rows per
+// lane are in flight.  Rows are added in key order as terms of the bag's
+// cascaded compensated sum, two columns per instruction; a skipped key or a
+// position past the bag adds an exact zero, which leaves the sum unchanged.
+// The result is scaled for mean pooling and stored into the bag's output
+// slice.  kInfer: the inference forward -- a key whose row is in the table's
+// fp16 cache travels as its cache slot (kCacheBit set) and its 4 fp16 columns
+// are copied instead of the table's; no ids are written.
+template <int LR, int DT, int SLOT, bool kInfer>
 __device__ __forceinline__ void pool_bags_ring(const FwdArgs& a, const TableDev& tb, const int64_t* kp, int li,
                                                uint32_t gmask, int64_t j0, int nbg, int my_start, int my_end,
                                                bool my_tid_ok, bool colok, float* out_col, int64_t bg0,
@@ -293,15 +191,25 @@ __device__ __forceinline__ void pool_bags_ring(const FwdArgs& a, const TableDev&
                 if (p < e0) {
                     const int64_t key = __ldg(kp + p);
                     const bool valid = tok && key >= 0 && key < tb.rows;
-                    if (a.write_ids) {
+                    if (!kInfer && a.write_ids) {
                         a.gid_out[p] = valid ? tb.row_base + (uint32_t)key : a.sentinel;
                         a.bag_out[p] = (uint32_t)(j0 + k);
                     }
-                    if (!valid && tok) atomicOr(a.err, ERRBIT_KEY_RANGE);
-                    if (valid) kk[j] = (uint32_t)key;
+                    // the inference forward skips a dynamic table's unseen ids silently
+                    if (!valid && tok && !(kInfer && tb.dynamic)) atomicOr(a.err, ERRBIT_KEY_RANGE);
+                    if (valid) {
+                        kk[j] = (uint32_t)key;
+                        // a cached row travels as its cache slot with kCacheBit set
+                        // (tables with a cache have fewer than 2^31 rows)
+                        if (kInfer && tb.cache_map) {
+                            const int64_t cs = cache_slot_of(tb, key);
+                            if (cs >= 0) kk[j] = kCacheBit | (uint32_t)cs;
+                        }
+                    }
                 }
             }
             const int n = e0 - w < WIN ? e0 - w : WIN;
+            uint32_t cached = 0;   // inference: bit q set when key q's row comes from the cache
             // batch b (keys 8b .. 8b+7 of the window) goes to slots 8*(b&1) ..
             auto request = [&](int b) {
 #pragma unroll
@@ -309,8 +217,13 @@ __device__ __forceinline__ void pool_bags_ring(const FwdArgs& a, const TableDev&
                     const int q = b * kRingBatch + u;
                     const uint32_t kq = __shfl_sync(gmask, kk[q / LR], q % LR, LR);
                     const bool live = q < n && kq != kNoRow && colok;
-                    ring_copy(ring + (uint32_t)((b & 1) * kRingBatch + u) * kSlot,
-                              live ? wlane + (uint64_t)kq * rbytes : wlane, F32, live);
+                    const uint32_t dst = ring + (uint32_t)((b & 1) * kRingBatch + u) * kSlot;
+                    if (kInfer && live && (kq & kCacheBit)) {
+                        ring_copy8(dst, tb.cache_w + (int64_t)(kq & ~kCacheBit) * tb.dim + 4 * li);
+                        cached |= 1u << q;
+                    } else {
+                        ring_copy(dst, live ? wlane + (uint64_t)kq * rbytes : wlane, F32, live);
+                    }
                 }
                 ring_commit();
             };
@@ -324,7 +237,11 @@ __device__ __forceinline__ void pool_bags_ring(const FwdArgs& a, const TableDev&
 #pragma unroll
                 for (int u = 0; u < kRingBatch; ++u) {
                     float4 x;
-                    if constexpr (F32) {
+                    if (kInfer && ((cached >> (b * kRingBatch + u)) & 1u)) {
+                        uint2 r;
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(base + (uint32_t)u * kSlot));
+                        x = bits16_to_f32(r, EMB_F16);
+                    } else if constexpr (F32) {
                         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                                      : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
                                      : "r"(base + (uint32_t)u * kSlot));
@@ -358,12 +275,9 @@ __device__ __forceinline__ void pool_bags_lr(int Lr, const FwdArgs& a, const Tab
                                              uint32_t gmask, int64_t j0, int nbg, int my_start, int my_end,
                                              bool my_tid_ok, bool colok, float* out_col, int64_t bg0, uint32_t ring)
 {
-#define POOL(LR)                                                                                                     \
-    if constexpr (kInfer)                                                                                            \
-        pool_bags<LR, kInfer, DT>(a, tb, kp, li, gmask, j0, nbg, my_start, my_end, my_tid_ok, colok, out_col, bg0); \
-    else                                                                                                             \
-        pool_bags_ring<LR, DT, SLOT>(a, tb, kp, li, gmask, j0, nbg, my_start, my_end, my_tid_ok, colok, out_col, bg0, \
-                                     ring)
+#define POOL(LR)                                                                                                  \
+    pool_bags_ring<LR, DT, SLOT, kInfer>(a, tb, kp, li, gmask, j0, nbg, my_start, my_end, my_tid_ok, colok, out_col, \
+                                         bg0, ring)
     switch (Lr) {
         case 1: POOL(1); break;
         case 2: POOL(2); break;
@@ -564,18 +478,11 @@ int launch_forward(const FwdArgs& a, cudaStream_t st)
     const int64_t warps = a.warps_per_table * a.num_tables;
     if (warps <= 0) return 0;
     const unsigned blocks = (unsigned)((warps * 32 + kThreads - 1) / kThreads);
-    if (a.infer) {
-        if (a.rows16)
-            fwd_pool<kBlocks16, true><<<blocks, kThreads, 0, st>>>(a);
-        else
-            fwd_pool<3, true><<<blocks, kThreads, 0, st>>>(a);
-    } else {
-        auto kernel = a.rows16 ? fwd_pool<kBlocks16, false> : fwd_pool<3, false>;
-        const int smem = ring_bytes(a.rows16 ? 8 : 16);
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return -1;
-        kernel<<<blocks, kThreads, smem, st>>>(a);
-    }
+    auto kernel = a.infer ? (a.rows16 ? fwd_pool<kBlocks16, true> : fwd_pool<3, true>)
+                          : (a.rows16 ? fwd_pool<kBlocks16, false> : fwd_pool<3, false>);
+    const int smem = ring_bytes(a.rows16 ? 8 : 16);
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+    kernel<<<blocks, kThreads, smem, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

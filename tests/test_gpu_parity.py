@@ -649,13 +649,25 @@ def test_dynamic_table_full_and_reserved_key_are_reported():
 # inference forward with fp16 caches of hot rows
 # ---------------------------------------------------------------------------
 
-def test_forward_infer_with_caches():
+# "mixed": fp32 and 16-bit tables (16-byte ring slots), short bags;
+# "rows16": 16-bit tables only (the 8-byte-slot kernel), bags of up to 74 keys
+# (several key windows, cached rows in every batch of a window)
+INFER_CASES = {
+    "mixed": ([ci.TableSpec(3000, 128, "f32", "sum", "adagrad"), ci.TableSpec(900, 16, "bf16", "mean", "sgd"),
+               ci.TableSpec(500, 64, "f16", "sum", "sgd"), ci.TableSpec(60, 20, "f32", "mean", "sgd")], 700, 7,
+              {0: np.arange(30), 1: np.array([2, 2, 5, 899, 800, 3]), 3: np.arange(60)}),
+    "rows16": ([ci.TableSpec(2000, 64, "f16", "sum", "sgd"), ci.TableSpec(700, 8, "bf16", "mean", "sgd"),
+                ci.TableSpec(300, 128, "f16", "mean", "adagrad")], 300, 75,
+               {0: np.arange(40), 2: np.array([2, 7, 299])}),
+}
+
+
+@pytest.mark.parametrize("case", sorted(INFER_CASES))
+def test_forward_infer_with_caches(case):
     import torch
     from dlrm_sparse_embedding_gb300 import EMB_ERR_KEY_RANGE, EMB_OK, EmbeddingLayer
-    tabs = [ci.TableSpec(3000, 128, "f32", "sum", "adagrad"), ci.TableSpec(900, 16, "bf16", "mean", "sgd"),
-            ci.TableSpec(500, 64, "f16", "sum", "sgd"), ci.TableSpec(60, 20, "f32", "mean", "sgd")]
-    B = 700
-    lens = np.random.default_rng(31).integers(0, 7, size=len(tabs) * B)
+    tabs, B, max_len, cached = INFER_CASES[case]
+    lens = np.random.default_rng(31).integers(0, max_len, size=len(tabs) * B)
 
     def keys(rng, t, s, L):
         k = rng.integers(0, s.rows, L)
@@ -663,7 +675,6 @@ def test_forward_infer_with_caches():
         return k
 
     w, b, _ = _custom(tabs, B, lens, keys, seed=32)
-    cached = {0: np.arange(30), 1: np.array([2, 2, 5, 899, 800, 3]), 3: np.arange(60)}
     seed = 0
     layer = EmbeddingLayer(w.tables, B, b.nnz)
     try:
@@ -686,7 +697,7 @@ def test_forward_infer_with_caches():
             layer.cache_build(t, torch.zeros(0, dtype=torch.int64).cuda())
         assert max_rel_err(layer.forward_infer(k, o, tid, B).cpu().numpy(), want0, scale0) <= 1e-5
         # a row id outside the table is reported
-        layer.cache_build(2, torch.tensor([1, 500], dtype=torch.int64).cuda())
+        layer.cache_build(1, torch.tensor([1, tabs[1].rows], dtype=torch.int64).cuda())
         assert layer.sync_status() == EMB_ERR_KEY_RANGE
     finally:
         layer.close()

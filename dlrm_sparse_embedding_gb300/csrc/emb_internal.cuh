@@ -143,17 +143,36 @@ __device__ __forceinline__ void store_w4(void* w, int dtype, int64_t elem, float
     *reinterpret_cast<uint2*>(static_cast<unsigned short*>(w) + elem) = raw;
 }
 
+// What every table of a layer has in common, fixed at compile time where the
+// layer is uniform (-1: read from each table's descriptor at run time).
+template <int OPT, int DT, int POOL, int MASTER>
+struct LayerSpec {
+    static constexpr int kOpt = OPT, kDt = DT, kPool = POOL, kMaster = MASTER;
+};
+using AnyLayer = LayerSpec<-1, -1, -1, -1>;
+
+template <class S>
+__device__ __forceinline__ int opt_of(const TableDev& tb) { return S::kOpt >= 0 ? S::kOpt : tb.opt; }
+template <class S>
+__device__ __forceinline__ int dtype_of(const TableDev& tb) { return S::kDt >= 0 ? S::kDt : tb.dtype; }
+template <class S>
+__device__ __forceinline__ bool mean_of(const TableDev& tb) { return (S::kPool >= 0 ? S::kPool : tb.pooling) == EMB_POOL_MEAN; }
+template <class S>
+__device__ __forceinline__ float* master_of(const TableDev& tb) { return S::kMaster == 0 ? nullptr : tb.master; }
+
 // One optimizer step on 4 consecutive elements (starting at elem) of row
 // `row`, whose current values have been loaded: w (from load_update_w4), and
 // the state a from load_state4.  A table with a master copy gets the new
 // fp32 values there and their nearest-even rounding in the stored row.  ssq is the sum over the whole row of G^2 (row-wise Adagrad
 // only; the caller reduces it over the lanes holding the row), and `writer`
 // says which one lane stores the row's accumulator.
+template <class S = AnyLayer>
 __device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t row, int64_t elem, const float g[4],
                                               float4 w, float4 a, float ssq, bool writer)
 {
     float wv[4] = {w.x, w.y, w.z, w.w};
-    if (tb.opt == EMB_OPT_ADAGRAD) {
+    const int opt = opt_of<S>(tb);
+    if (opt == EMB_OPT_ADAGRAD) {
         float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -162,7 +181,7 @@ __device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t row, i
             wv[q] = __fmaf_rn(-tb.lr, __fdiv_rn(g[q], den), wv[q]);
         }
         *reinterpret_cast<float4*>(tb.state + elem) = make_float4(av[0], av[1], av[2], av[3]);
-    } else if (tb.opt == EMB_OPT_ROWWISE_ADAGRAD) {
+    } else if (opt == EMB_OPT_ROWWISE_ADAGRAD) {
         const float an = __fadd_rn(a.x, __fdiv_rn(ssq, (float)tb.dim));
         const float den = __fadd_rn(__fsqrt_rn(an), tb.eps);
 #pragma unroll
@@ -172,24 +191,29 @@ __device__ __forceinline__ void apply_update4(const TableDev& tb, int64_t row, i
 #pragma unroll
         for (int q = 0; q < 4; ++q) wv[q] = __fmaf_rn(-tb.lr, g[q], wv[q]);
     }
-    if (tb.master) *reinterpret_cast<float4*>(tb.master + elem) = make_float4(wv[0], wv[1], wv[2], wv[3]);
-    store_w4(tb.w, tb.dtype, elem, make_float4(wv[0], wv[1], wv[2], wv[3]));
+    float* const master = master_of<S>(tb);
+    if (master) *reinterpret_cast<float4*>(master + elem) = make_float4(wv[0], wv[1], wv[2], wv[3]);
+    store_w4(tb.w, dtype_of<S>(tb), elem, make_float4(wv[0], wv[1], wv[2], wv[3]));
 }
 
 // The weights an update starts from: the fp32 master when the table has one,
 // else the stored row.
+template <class S = AnyLayer>
 __device__ __forceinline__ float4 load_update_w4(const TableDev& tb, int64_t elem)
 {
-    if (tb.master) return *reinterpret_cast<const float4*>(tb.master + elem);
-    return load_w4(tb.w, tb.dtype, elem);
+    const float* master = master_of<S>(tb);
+    if (master) return *reinterpret_cast<const float4*>(master + elem);
+    return load_w4(tb.w, dtype_of<S>(tb), elem);
 }
 
 // Optimizer state of the 4 elements at elem of row `row`: Adagrad's four
 // accumulators, row-wise Adagrad's one (in .x), nothing for SGD.
+template <class S = AnyLayer>
 __device__ __forceinline__ float4 load_state4(const TableDev& tb, int64_t row, int64_t elem)
 {
-    if (tb.opt == EMB_OPT_ADAGRAD) return *reinterpret_cast<const float4*>(tb.state + elem);
-    if (tb.opt == EMB_OPT_ROWWISE_ADAGRAD) return make_float4(tb.state[row], 0.f, 0.f, 0.f);
+    const int opt = opt_of<S>(tb);
+    if (opt == EMB_OPT_ADAGRAD) return *reinterpret_cast<const float4*>(tb.state + elem);
+    if (opt == EMB_OPT_ROWWISE_ADAGRAD) return make_float4(tb.state[row], 0.f, 0.f, 0.f);
     return make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
@@ -334,6 +358,7 @@ struct ReduceArgs {
                                 // rows split over many chunks from the back)
     int* split_count;           // [4] entries of the two lists, then the combine's work counters
     int32_t max_dim;            // widest table of the layer (selects the chunk kernel's occupancy)
+    int32_t uni_opt, uni_dtype, uni_pool, uni_master;   // shared by every table, or -1 (selects a specialised kernel)
     int* err;
 };
 

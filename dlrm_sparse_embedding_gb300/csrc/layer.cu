@@ -23,6 +23,7 @@ struct emb_layer {
     uint64_t total_rows = 0;
     int64_t total_dim = 0;
     int32_t maxdim = 0;
+    int64_t test_chunk = 0;   // EMB_TEST_REDUCE_CHUNK (0: unset)
 
     // forward -> backward
     uint32_t* gid = nullptr;
@@ -109,11 +110,23 @@ constexpr int64_t kMinChunk = 32, kMaxChunk = 256;
 
 // Nominal lookups per warp in the segmented reduction: enough chunks to fill
 // the GPU, at most kMaxChunk so a warp's run list fits in shared memory.
-int64_t chunk_for(int64_t n)
+// Nominal lookups per reduction chunk: the smallest power of two in
+// [kMinChunk, kMaxChunk] giving at most kTargetChunks chunks.  Tests may
+// raise it (EMB_TEST_REDUCE_CHUNK, a power of two in that range, read by
+// emb_create) to run the multi-hot chunk kernels on small inputs.
+int64_t chunk_for(int64_t n, int64_t at_least = 0)
 {
     int64_t c = kMinChunk;
-    while (c < kMaxChunk && c * kTargetChunks < n) c <<= 1;
+    while (c < kMaxChunk && (c * kTargetChunks < n || c < at_least)) c <<= 1;
     return c;
+}
+
+int64_t test_reduce_chunk()
+{
+    const char* v = std::getenv("EMB_TEST_REDUCE_CHUNK");
+    if (!v) return 0;
+    const long long c = std::strtoll(v, nullptr, 10);
+    return (c >= kMinChunk && c <= kMaxChunk && (c & (c - 1)) == 0) ? (int64_t)c : 0;
 }
 
 int64_t nchunks_bound(int64_t max_nnz)
@@ -383,6 +396,7 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
     L->total_rows = total_rows;
     L->total_dim = total_dim;
     L->maxdim = maxdim;
+    L->test_chunk = test_reduce_chunk();
 
     bool ok = true;
     uint64_t rb = 0;
@@ -705,7 +719,7 @@ int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, vo
     const int64_t n = L->last_nnz;
     ReduceArgs r{};
     r.n = n;
-    r.chunk = chunk_for(n);
+    r.chunk = chunk_for(n, L->test_chunk);
     r.nchunks = (n + r.chunk - 1) / r.chunk;
     r.tables = L->d_tables;
     r.num_tables = L->T;
@@ -717,6 +731,16 @@ int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, vo
     r.split_list = L->split_list;
     r.split_count = L->split_count;
     r.max_dim = L->maxdim;
+    r.uni_opt = L->tabs[0].opt;
+    r.uni_dtype = L->tabs[0].dtype;
+    r.uni_pool = L->tabs[0].pooling;
+    r.uni_master = L->tabs[0].master ? 1 : 0;
+    for (const TableDev& d : L->tabs) {
+        if (d.opt != r.uni_opt) r.uni_opt = -1;
+        if (d.dtype != r.uni_dtype) r.uni_dtype = -1;
+        if (d.pooling != r.uni_pool) r.uni_pool = -1;
+        if ((d.master ? 1 : 0) != r.uni_master) r.uni_master = -1;
+    }
     r.err = L->err;
     int rc = EMB_OK;
     L->dedup_valid = false;

@@ -232,6 +232,37 @@ def test_odd_dims_and_last_rows(variant):
     check_step(w, b, g, variant)
 
 
+# Layers whose tables share one storage type, optimizer and pooling run a
+# reduction kernel specialised for that combination: every combination, with
+# the chunk length small inputs get (32 lookups) and, forced through the
+# library's test hook, the multi-hot one (256 lookups, key windows staged in
+# shared memory).  A hot row spans several chunks (split runs and one-run
+# chunks) and bags repeat rows (entries of multiplicity above one).
+UNIFORM_SPECS = [(dt, opt, pool) for dt in ("f32", "f16", "bf16")
+                 for opt in ("sgd", "adagrad", "rowwise_adagrad") for pool in ("sum", "mean")]
+
+
+@pytest.mark.parametrize("chunk", [0, 256])
+@pytest.mark.parametrize("variant", ["reduction", "unique_sort"])
+@pytest.mark.parametrize("dt,opt,pool", UNIFORM_SPECS)
+def test_uniform_layer_kernels(dt, opt, pool, variant, chunk, monkeypatch):
+    if chunk:
+        monkeypatch.setenv("EMB_TEST_REDUCE_CHUNK", str(chunk))
+    else:
+        monkeypatch.delenv("EMB_TEST_REDUCE_CHUNK", raising=False)
+    tabs = [ci.TableSpec(r, d, dt, pool, opt) for r, d in ((1500, 16), (700, 64), (300, 128))]
+    B = 300
+    lens = np.random.default_rng(61).integers(0, 45, size=len(tabs) * B)
+
+    def keys(rng, t, s, L):
+        k = rng.integers(0, s.rows, L)
+        k[rng.random(L) < 0.25] = 3                         # a row hit about 2 000 times per table
+        return k
+
+    w, b, g = _custom(tabs, B, lens, keys, seed=62, name="uniform_%s_%s_%s" % (dt, opt, pool))
+    check_step(w, b, g, variant)
+
+
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_out_of_range_keys_are_skipped_and_reported(variant):
     from dlrm_sparse_embedding_gb300 import EMB_ERR_KEY_RANGE

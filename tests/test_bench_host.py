@@ -100,7 +100,11 @@ def test_recorded_traffic_only_while_the_kernel_source_is_unchanged(tmp_path):
 def test_committed_traffic_record_names_the_reduction_sources():
     with open(os.path.join(bench.ROOT, "profiles", "traffic_multihot_reduction.json")) as f:
         rec = json.load(f)["reduce_update"]
+    # the reduction's sources: the combine and launch, the chunk kernel, its
+    # fp32 specialisations (the multi-hot layer is uniform fp32), shared helpers
     assert set(rec["sources_sha256"]) == {"dlrm_sparse_embedding_gb300/csrc/update.cu",
+                                          "dlrm_sparse_embedding_gb300/csrc/reduce_chunks.cuh",
+                                          "dlrm_sparse_embedding_gb300/csrc/update_f32.cu",
                                           "dlrm_sparse_embedding_gb300/csrc/emb_internal.cuh"}
     assert rec["traffic_bytes"] == sum(k["read"] + k["write"] for k in rec["per_kernel"].values())
 

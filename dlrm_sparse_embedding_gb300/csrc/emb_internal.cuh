@@ -357,6 +357,7 @@ struct ReduceArgs {
     uint32_t* split_list;       // [nchunks] chunks where a split run starts (short rows from the front,
                                 // rows split over many chunks from the back)
     int* split_count;           // [4] entries of the two lists, then the combine's work counters
+    int* long_done;             // [nchunks] segments finished per long split run (zero between backwards)
     int32_t max_dim;            // widest table of the layer (selects the chunk kernel's occupancy)
     int32_t uni_opt, uni_dtype, uni_pool, uni_master;   // shared by every table, or -1 (selects a specialised kernel)
     int* err;

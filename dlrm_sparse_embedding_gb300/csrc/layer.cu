@@ -52,6 +52,7 @@ struct emb_layer {
     float* slots = nullptr;
     uint32_t* split_list = nullptr;
     int* split_count = nullptr;
+    int* long_done = nullptr;
     int64_t nchunks_max = 0;
     int* err = nullptr;
     int64_t* scratch64 = nullptr;   // [2]: num-unique copy target, misc
@@ -460,6 +461,7 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
          dalloc_n(L, &L->ukey_s, L->max_unique) && dalloc_n(L, &L->uslot_s, L->max_unique) &&
          dalloc_n(L, &L->bits_dev, 1) && dalloc_n(L, &L->slots, L->nchunks_max * 2 * kMaxDim) &&
          dalloc_n(L, &L->split_list, L->nchunks_max) && dalloc_n(L, &L->split_count, 4) &&
+         dalloc_n(L, &L->long_done, L->nchunks_max) &&
          dalloc_n(L, &L->err, 1) && dalloc_n(L, &L->scratch64, 2) && dalloc_n(L, &L->d_init_acc, num_tables);
     std::vector<int32_t> dyn;
     std::vector<float> init_acc(num_tables);
@@ -475,6 +477,7 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
                  cudaSuccess &&
              cudaMemset(L->htable, 0xFF, sizeof(uint32_t) * cap) == cudaSuccess &&
              cudaMemset(L->err, 0, sizeof(int)) == cudaSuccess &&
+             cudaMemset(L->long_done, 0, sizeof(int) * L->nchunks_max) == cudaSuccess &&
              cudaMemcpy(L->d_init_acc, init_acc.data(), sizeof(float) * num_tables, cudaMemcpyHostToDevice) ==
                  cudaSuccess &&
              (L->num_dyn == 0 || cudaMemcpy(L->d_dyn_tables, dyn.data(), sizeof(int32_t) * L->num_dyn,
@@ -730,6 +733,7 @@ int emb_backward_update(emb_layer* L, const float* grad_out, int32_t variant, vo
     r.slots = L->slots;
     r.split_list = L->split_list;
     r.split_count = L->split_count;
+    r.long_done = L->long_done;
     r.max_dim = L->maxdim;
     r.uni_opt = L->tabs[0].opt;
     r.uni_dtype = L->tabs[0].dtype;

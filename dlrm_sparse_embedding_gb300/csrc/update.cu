@@ -40,7 +40,7 @@ constexpr int kCombineThreads = 1024;   // combine block: all warps on a long ro
 constexpr int kCombineGroups = 4;
 constexpr int kCombineBlocksPerSM = 1;   // one 1024-thread block per SM
 constexpr int kLongSegs = 32;            // blocks sharing one long split run ...
-constexpr int kSegPieces = 256;          // ... each adding at least this many of its pieces
+constexpr int kSegPieces = 1024;         // ... each adding at least this many of its pieces
 
 // Barrier over `nthr` threads (a multiple of 32) on named barrier `bar`,
 // returning how many of them passed pred.
@@ -166,7 +166,8 @@ __device__ __forceinline__ void combine_run(const ReduceArgs& a, int64_t c, int6
 
 // Segment `seg` of the long split run registered as long item `item`, by the
 // whole block.  The run's pieces are cut into nseg = min(kLongSegs,
-// max(1, P / kSegPieces)) equal ranges, each summed by one block; the block
+// max(1, P / kSegPieces)) equal ranges, each summed by one block (one segment:
+// the block applies the update at once); otherwise the block
 // that finishes a run's last outstanding segment (a counter per item, reset
 // by that block) adds the segment sums in segment order and applies the
 // update.  The run's extent comes from a kCombineThreads-ary search over the
@@ -184,7 +185,11 @@ __device__ __forceinline__ void combine_long_segment(const ReduceArgs& a, int it
     // more, i.e. it still continues past chunk c + (seg + 1) * kSegPieces - 3:
     // one probe spares the search for the segments a shorter run does not have
     if (seg > 0) {
-        if (tid == 0) *s_flag = next_chunk_continues(a, c + (int64_t)(seg + 1) * kSegPieces - 3, key);
+        if (tid == 0) {
+            *s_flag = next_chunk_continues(a, c + (int64_t)(seg + 1) * kSegPieces - 3, key);
+            // the run's later segments do not exist either: the work counter skips them
+            if (!*s_flag) atomicMax(a.split_count + 2, (item + 1) * kLongSegs);
+        }
         group_sync(0, T);
         if (!*s_flag) return;
     }
@@ -208,6 +213,10 @@ __device__ __forceinline__ void combine_long_segment(const ReduceArgs& a, int it
     const int64_t q0 = (int64_t)seg * P / nseg, q1 = (int64_t)(seg + 1) * P / nseg;
     float g[4];
     sum_pieces(a, c, q0, q1, colok, part, 0, T, tid, 0, g);
+    if (nseg == 1) {   // the whole run in one segment
+        if (tid < 32) apply_row(a, tb, key, g, lane, colok);
+        return;
+    }
     // the segment's sum replaces its first piece, which only this block read
     if (tid < 32 && colok) *reinterpret_cast<float4*>(const_cast<float*>(piece_ptr(a, c, q0)) + 4 * lane) =
         make_float4(g[0], g[1], g[2], g[3]);

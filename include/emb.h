@@ -117,7 +117,12 @@ typedef struct emb_layer emb_layer;   /* opaque; owns tables, optimizer state an
  * here, once, so the step itself allocates nothing.  Weights are NOT
  * initialised (call emb_init_uniform or emb_set_rows).  On success *out owns
  * the device memory until emb_destroy.  Allocation failure: EMB_ERR_OOM with
- * nothing leaked and *out untouched. */
+ * nothing leaked and *out untouched.
+ * Test hooks, read here from the environment (unset in normal use):
+ * EMB_TEST_ALLOC_LIMIT_BYTES caps what this call may allocate (to reach the
+ * EMB_ERR_OOM path); EMB_TEST_REDUCE_CHUNK (a power of two in [32, 256])
+ * raises the layer's reduction chunk length, so small inputs run the kernels
+ * large multi-hot inputs get.  Neither changes any result. */
 int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batch,
                int64_t max_nnz, emb_layer** out);
 

@@ -357,7 +357,8 @@ def run_reference(args, w: ci.Workload):
         "data": "synthetic", "config": {"workload": CONFIG_TEXT[args.config], "batch": sb_n, "nnz": int(sb.nnz),
                                         "sample_of_batch": w.batch,
                                         "variant": "definition (no dedup variant)"},
-        "cpu_baseline": {"value": v, "unit": "lookups/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "lookups/s", "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": v, "unit": "lookups/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -597,7 +598,8 @@ def main():
         t_start = time.perf_counter()
         while not secs or (time.perf_counter() - t_start < 10.0 and len(secs) < 20):
             secs.append(oracle_step_timed(sw, sb, sg, w.seed))
-        cpu = {"value": sb.nnz / (sum(secs) / len(secs)), "unit": "lookups/s", "cores": 1, "kind": "oracle",
+        cpu = {"value": sb.nnz / (sum(secs) / len(secs)), "unit": "lookups/s", "cores": 1,
+               "host_cores": os.cpu_count(), "kind": "oracle",
                "sample": "%d of the %d samples (%d lookups), full step a1..a5, mean of %d runs" % (
                    sb_n, w.batch, sb.nnz, len(secs))}
 

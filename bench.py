@@ -507,8 +507,12 @@ def main():
     # ---- end to end: host buffers, copies inside the timed region ----
     # Every step copies its inputs (keys, offsets, table ids, grad_out) from
     # pinned host memory and reads the pooled output back.  The copies run on
-    # their own streams, double-buffered, so step i's compute overlaps the
-    # upload of step i+1 and the download of step i-1.
+    # their own streams, double-buffered: while step i computes, the inputs of
+    # step i+1 go up, and step i's output comes down as soon as its forward
+    # is done.  The pipeline runs on from the warm-up into the timed steps, so
+    # the timed region holds K uploads (those of the steps after the first
+    # timed one, the first's having gone up during the last warm-up step) and
+    # K downloads: the bytes of K steps, at the pipeline's steady rate.
     e2e = None
     if not args.no_e2e:
         hk = [torch.from_numpy(b.keys).pin_memory() for b in batches]
@@ -522,6 +526,7 @@ def main():
         comp = torch.cuda.current_stream()
         s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
         ev_up = [torch.cuda.Event() for _ in range(2)]
+        ev_fwd = [torch.cuda.Event() for _ in range(2)]
         ev_comp = [torch.cuda.Event() for _ in range(2)]
         ev_down = [torch.cuda.Event() for _ in range(2)]
 
@@ -536,31 +541,33 @@ def main():
                 dbuf[b]["g"].copy_(hg, non_blocking=True)
                 ev_up[b].record(s_up)
 
-        def run_e2e(nsteps):
-            upload(0)
-            for i in range(nsteps):
-                b, k = i % 2, i % args.batches
-                n = hk[k].numel()
-                if i + 1 < nsteps:
-                    upload(i + 1)
-                comp.wait_event(ev_up[b])
-                comp.wait_event(ev_down[b])          # output buffer b has been read back
-                layer.forward(dbuf[b]["k"][:n], dbuf[b]["o"], dbuf[b]["t"], w.batch, dbuf[b]["out"])
-                layer.backward_update(dbuf[b]["g"], args.variant)
-                ev_comp[b].record(comp)
-                with torch.cuda.stream(s_down):
-                    s_down.wait_event(ev_comp[b])
-                    hout[b].copy_(dbuf[b]["out"], non_blocking=True)
-                    ev_down[b].record(s_down)
-            comp.wait_stream(s_down)
+        def e2e_step(i):
+            b, k = i % 2, i % args.batches
+            n = hk[k].numel()
+            upload(i + 1)
+            comp.wait_event(ev_up[b])
+            comp.wait_event(ev_down[b])              # output buffer b has been read back
+            layer.forward(dbuf[b]["k"][:n], dbuf[b]["o"], dbuf[b]["t"], w.batch, dbuf[b]["out"])
+            ev_fwd[b].record(comp)
+            layer.backward_update(dbuf[b]["g"], args.variant)
+            ev_comp[b].record(comp)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(ev_fwd[b])
+                hout[b].copy_(dbuf[b]["out"], non_blocking=True)
+                ev_down[b].record(s_down)
 
-        run_e2e(args.warmup)
+        upload(0)
+        for i in range(args.warmup):
+            e2e_step(i)
         torch.cuda.synchronize()
         if ws > 1:
             dist.barrier(device_ids=[local])
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         f0.record(comp)
-        run_e2e(args.steps)
+        for i in range(args.warmup, args.warmup + args.steps):
+            e2e_step(i)
+        comp.wait_stream(s_down)
+        comp.wait_stream(s_up)
         f1.record(comp)
         torch.cuda.synchronize()
         ems = f0.elapsed_time(f1) / args.steps
@@ -569,7 +576,8 @@ def main():
         d2h = w.batch * w.total_dim * 4
         e2e = {"value": whole_job_rate(batches[0].nnz, ws, ems), "unit": "lookups/s", "ms_per_step": ems,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "copies": "pinned host <-> device, double-buffered on two copy streams overlapping compute"}
+               "copies": "pinned host <-> device, double-buffered on two copy streams overlapping compute; "
+                         "steady state: K uploads and K downloads inside the K timed steps"}
 
     layer.close()
     if rank != 0:

@@ -291,14 +291,16 @@ __device__ __forceinline__ TileLoc locate_tile(const SortScratch& sc, int64_t ti
     return t;
 }
 
-template <typename K>
+// NB: the digit count when fixed at compile time (256 or 1024, the digit
+// widths of the common key sizes), 0 when read from the arguments.
+template <typename K, int NB>
 __global__ void __launch_bounds__(kSortThreads) sort_upsweep(SortArgs a, SortScratch sc, int pass)
 {
     PassCtx c = pass_ctx(a, pass);
     const int64_t tile = blockIdx.x;
     if (!c.active || tile >= sc.seg_tile0[a.num_seg]) return;
     __shared__ uint32_t hist[1 << kMaxDigitBits];
-    const int nb = 1 << a.D;
+    const int nb = NB > 0 ? NB : 1 << a.D;
     for (int i = threadIdx.x; i < nb; i += kSortThreads) hist[i] = 0;
     const TileLoc tl = locate_tile(sc, tile);
     __syncthreads();
@@ -487,7 +489,7 @@ __device__ __forceinline__ void load_tile_items(const K* src_k, const uint32_t* 
 // ...); while a tile is ranked and scattered, the next tile's items are
 // already requested (its descriptor one tile earlier still), so the load
 // latency hides behind the work.
-template <typename K>
+template <typename K, int NB>
 __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep(SortArgs a, SortScratch sc, int pass)
 {
     PassCtx c = pass_ctx(a, pass);
@@ -505,7 +507,7 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
     else { src_k = static_cast<const K*>(a.keys_out); src_v = a.vals_out; }
 
     constexpr int kWarps = kDownThreads / 32;
-    const int nb = 1 << a.D;
+    const int nb = NB > 0 ? NB : 1 << a.D;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // the per-warp lane masks of each digit (zero between ranking steps), then
     // the tile's keys and values in their in-tile sorted order
@@ -787,8 +789,18 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
     const int nb = 1 << plan.digit_bits;
     const size_t smem = sort_region0_bytes(sizeof(K), nb) + sizeof(uint32_t) * 2 * (size_t)nb +
                         sizeof(uint16_t) * (size_t)(kDownThreads / 32) * nb;
-    if (cudaFuncSetAttribute(sort_downsweep<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-        cudaFuncSetAttribute(sort_downsweep<K>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    // the histogram and ranking kernels with the digit count fixed where it is 256 or 1024
+    void (*upsweep)(SortArgs, SortScratch, int) = sort_upsweep<K, 0>;
+    void (*downsweep)(SortArgs, SortScratch, int) = sort_downsweep<K, 0>;
+    if (nb == 256) {
+        upsweep = sort_upsweep<K, 256>;
+        downsweep = sort_downsweep<K, 256>;
+    } else if (nb == 1024) {
+        upsweep = sort_upsweep<K, 1024>;
+        downsweep = sort_downsweep<K, 1024>;
+    }
+    if (cudaFuncSetAttribute(downsweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(downsweep, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
         return -1;
     int dev = 0, sms = 152;
     cudaGetDevice(&dev);
@@ -800,7 +812,7 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
     sort_tiles<<<tile_blocks, 256, 0, st>>>(a, sc, tiles);
     int launched = 2;
     for (int p = 0; p < plan.passes_max; ++p) {
-        sort_upsweep<K><<<(unsigned)tiles, kSortThreads, 0, st>>>(a, sc, p);
+        upsweep<<<(unsigned)tiles, kSortThreads, 0, st>>>(a, sc, p);
         sort_scan_groups<<<(unsigned)groups, kSortThreads, 0, st>>>(a, sc, p);
         sort_scan_segments<<<dim3((unsigned)a.num_seg, (unsigned)((nb + 31) / 32)), kScanWarps * 32, 0, st>>>(a, sc, p);
         sort_seg_bases<<<(unsigned)a.num_seg, 1024, 0, st>>>(a, sc, p);
@@ -810,7 +822,7 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
             sort_scan_skips<<<1, kSetupThreads, 0, st>>>(a, sc, p);
             ++launched;
         }
-        sort_downsweep<K><<<ranking_blocks, kDownThreads, smem, st>>>(a, sc, p);
+        downsweep<<<ranking_blocks, kDownThreads, smem, st>>>(a, sc, p);
         ++launched;
     }
     if (cudaGetLastError() != cudaSuccess) return -1;

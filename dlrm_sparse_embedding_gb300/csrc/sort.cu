@@ -489,10 +489,16 @@ __device__ __forceinline__ void load_tile_items(const K* src_k, const uint32_t* 
 // ...); while a tile is ranked and scattered, the next tile's items are
 // already requested (its descriptor one tile earlier still), so the load
 // latency hides behind the work.
-template <typename K, int NB>
+template <typename K, int NB, int kRole>
 __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep(SortArgs a, SortScratch sc, int pass)
 {
     PassCtx c = pass_ctx(a, pass);
+    // kRole, when the host knows the number of passes: 1 first of several,
+    // 2 a middle pass, 3 the last of several, 4 the only pass (0: read from c)
+    if constexpr (kRole != 0) {
+        c.src_in = kRole == 1 || kRole == 4;
+        c.last = kRole == 3 || kRole == 4;
+    }
     const int64_t ntiles = sc.seg_tile0[a.num_seg];
     int64_t tile = blockIdx.x;
     if (!c.active || tile >= ntiles) return;
@@ -791,17 +797,35 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
                         sizeof(uint16_t) * (size_t)(kDownThreads / 32) * nb;
     // the histogram and ranking kernels with the digit count fixed where it is 256 or 1024
     void (*upsweep)(SortArgs, SortScratch, int) = sort_upsweep<K, 0>;
-    void (*downsweep)(SortArgs, SortScratch, int) = sort_downsweep<K, 0>;
+    void (*downsweep[5])(SortArgs, SortScratch, int) = {sort_downsweep<K, 0, 0>, sort_downsweep<K, 0, 0>,
+                                                        sort_downsweep<K, 0, 0>, sort_downsweep<K, 0, 0>,
+                                                        sort_downsweep<K, 0, 0>};
     if (nb == 256) {
         upsweep = sort_upsweep<K, 256>;
-        downsweep = sort_downsweep<K, 256>;
+        downsweep[0] = sort_downsweep<K, 256, 0>;
+        downsweep[1] = sort_downsweep<K, 256, 1>;
+        downsweep[2] = sort_downsweep<K, 256, 2>;
+        downsweep[3] = sort_downsweep<K, 256, 3>;
+        downsweep[4] = sort_downsweep<K, 256, 4>;
     } else if (nb == 1024) {
         upsweep = sort_upsweep<K, 1024>;
-        downsweep = sort_downsweep<K, 1024>;
+        downsweep[0] = sort_downsweep<K, 1024, 0>;
+        downsweep[1] = sort_downsweep<K, 1024, 1>;
+        downsweep[2] = sort_downsweep<K, 1024, 2>;
+        downsweep[3] = sort_downsweep<K, 1024, 3>;
+        downsweep[4] = sort_downsweep<K, 1024, 4>;
     }
-    if (cudaFuncSetAttribute(downsweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-        cudaFuncSetAttribute(downsweep, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-        return -1;
+    for (int r = 0; r < 5; ++r)
+        if (cudaFuncSetAttribute(downsweep[r], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+            cudaFuncSetAttribute(downsweep[r], cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+            return -1;
+    // the passes' roles are known here unless the significant bits live on the device
+    const int npe = (plan.bits_max + plan.digit_bits - 1) / plan.digit_bits;
+    auto role = [&](int p) {
+        if (a.bits_dev || npe != plan.passes_max) return 0;
+        if (npe == 1) return 4;
+        return p == 0 ? 1 : (p == npe - 1 ? 3 : 2);
+    };
     int dev = 0, sms = 152;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -822,7 +846,7 @@ int radix_sort_pairs(const SortPlan& plan, SortArgs a, void* scratch, cudaStream
             sort_scan_skips<<<1, kSetupThreads, 0, st>>>(a, sc, p);
             ++launched;
         }
-        downsweep<<<ranking_blocks, kDownThreads, smem, st>>>(a, sc, p);
+        downsweep[role(p)]<<<ranking_blocks, kDownThreads, smem, st>>>(a, sc, p);
         ++launched;
     }
     if (cudaGetLastError() != cudaSuccess) return -1;

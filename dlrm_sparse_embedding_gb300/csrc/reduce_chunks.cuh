@@ -84,9 +84,10 @@ __device__ __forceinline__ float entry_factor(const ReduceArgs& a, const uint16_
     return mean ? __fmul_rn(f, __ldg(a.bag_scale + b)) : f;
 }
 
-// kMinBlocks: resident blocks per SM the registers are sized for.  Layers
-// with rows wider than 64 run one lane group per warp and gain from more
-// warps in flight (10 blocks, 48 registers); narrower layers lose more to the
+// kMinBlocks: resident blocks per SM the registers are sized for.  One-hot
+// layers (short chunks) with rows wider than 64 run one lane group per warp
+// and gain from more warps in flight (10 blocks, 48 registers); narrower
+// rows, and multi-hot layers (key windows) of any width, lose more to the
 // spills than they gain (8 blocks, 64 registers).
 // kWindow: chunks of 128 lookups or more load their whole key window once
 // (faster on multi-hot layers, where chunks are long); short chunks find
@@ -342,13 +343,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) reduce_update_chunks(Red
     }
 }
 
-// The chunk kernel for layer spec S: occupancy by the widest row, key
-// windows for multi-hot chunk lengths.
+// The chunk kernel for layer spec S: key windows for multi-hot chunk
+// lengths; more resident blocks for one-hot layers of wide rows.
 template <class S>
 ChunkKernel chunks_kernel(const ReduceArgs& a)
 {
-    if (a.max_dim > 64) return a.chunk >= 128 ? reduce_update_chunks<10, true, S> : reduce_update_chunks<10, false, S>;
-    return a.chunk >= 128 ? reduce_update_chunks<8, true, S> : reduce_update_chunks<8, false, S>;
+    if (a.chunk >= 128) return reduce_update_chunks<8, true, S>;
+    return a.max_dim > 64 ? reduce_update_chunks<10, false, S> : reduce_update_chunks<8, false, S>;
 }
 
 // The chunk kernel specialised for storage type DT (master copies MASTER:

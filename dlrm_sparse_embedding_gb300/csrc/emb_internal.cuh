@@ -385,6 +385,8 @@ struct FwdArgs {
     bool rows16;                // every table stores 16-bit rows (selects the pooling kernel's occupancy)
     const int64_t* resolved;    // dynamic tables: row of each lookup (-1: none), read instead of keys
     bool infer;                 // the inference forward (reads caches, writes nothing for a backward)
+    int32_t* order_buf;         // [T] scratch for the tables' processing order, or null
+    const int32_t* order;       // set by launch_forward: table of each run of warps (null: table order)
     int* err;
 };
 

@@ -306,8 +306,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(fwd_ring) + threadIdx.x * kSlotBytes;
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int t = (int)(gw / a.warps_per_table);
-    if (t >= a.num_tables) return;
+    const int64_t slot = gw / a.warps_per_table;   // the slot-th table in processing order
+    if (slot >= a.num_tables) return;
+    const int t = a.order ? __ldg(a.order + slot) : (int)slot;
     const int64_t B = a.batch;
     const TableDev tb = a.tables[t];
     const int64_t* kp = tb.dynamic ? a.resolved : a.keys;   // a dynamic table's keys are resolved to rows
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
     const bool mean = tb.pooling == EMB_POOL_MEAN;
 
     // this group owns bags bg0 .. bg0+nbg-1 of table t; lane li describes bag li
-    const int64_t bg0 = (gw - (int64_t)t * a.warps_per_table) * 32 + (int64_t)g * Lr;
+    const int64_t bg0 = (gw - slot * a.warps_per_table) * 32 + (int64_t)g * Lr;
     const int64_t left = B - bg0;
     const int nbg = left <= 0 ? 0 : (left < Lr ? (int)left : Lr);
     if (nbg == 0) return;
@@ -414,6 +415,33 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
                                                    out_col, bg0, ring);
 }
 
+// The tables in descending order of their lookups in this batch (ties by
+// table index), for layers of at most kOrderThreads tables: one block; a
+// table's rank is the number of tables ahead of it.
+constexpr int kOrderThreads = 1024;
+
+__global__ void __launch_bounds__(kOrderThreads) fwd_order(FwdArgs a)
+{
+    __shared__ int64_t work[kOrderThreads];
+    const int T = a.num_tables;
+    for (int t = threadIdx.x; t < T; t += kOrderThreads) {
+        // clamped like the pooling kernel clamps them
+        const int64_t lo = clamp_offset(__ldg(a.offsets + (int64_t)t * a.batch), 0, a.nnz);
+        const int64_t hi = clamp_offset(__ldg(a.offsets + (int64_t)(t + 1) * a.batch), 0, a.nnz);
+        work[t] = hi > lo ? hi - lo : 0;
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < T; t += kOrderThreads) {
+        const int64_t wt = work[t];
+        int rank = 0;
+        for (int u = 0; u < T; ++u) {
+            const int64_t wu = work[u];
+            rank += (wu > wt || (wu == wt && u < t)) ? 1 : 0;
+        }
+        a.order_buf[rank] = t;
+    }
+}
+
 // Global row id and bag of every lookup, nothing else: the forward's id
 // output on its own, so the dedup can start while the pooling kernel runs.
 // A warp owns 32 consecutive bags of one table and streams their keys.
@@ -473,8 +501,9 @@ int launch_forward_ids(const FwdArgs& a, cudaStream_t st)
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
-int launch_forward(const FwdArgs& a, cudaStream_t st)
+int launch_forward(const FwdArgs& args, cudaStream_t st)
 {
+    FwdArgs a = args;
     const int64_t warps = a.warps_per_table * a.num_tables;
     if (warps <= 0) return 0;
     const unsigned blocks = (unsigned)((warps * 32 + kThreads - 1) / kThreads);
@@ -482,8 +511,18 @@ int launch_forward(const FwdArgs& a, cudaStream_t st)
                           : (a.rows16 ? fwd_pool<kBlocks16, false> : fwd_pool<3, false>);
     const int smem = ring_bytes(a.rows16 ? 8 : 16);
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
+    // multi-hot batches (more lookups than bags): tables with the most lookups
+    // first, so the block scheduler does not end on a heavy table's blocks
+    a.order = nullptr;
+    int launched = 1;
+    if (a.order_buf && a.num_tables >= 2 && a.num_tables <= kOrderThreads &&
+        a.nnz > (int64_t)a.num_tables * a.batch) {
+        fwd_order<<<1, kOrderThreads, 0, st>>>(a);
+        a.order = a.order_buf;
+        ++launched;
+    }
     kernel<<<blocks, kThreads, smem, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+    return cudaGetLastError() == cudaSuccess ? launched : -1;
 }
 
 }  // namespace emb

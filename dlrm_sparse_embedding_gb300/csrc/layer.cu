@@ -53,6 +53,7 @@ struct emb_layer {
     uint32_t* split_list = nullptr;
     int* split_count = nullptr;
     int* long_done = nullptr;
+    int32_t* table_order = nullptr;   // [T] the forward's table processing order
     int64_t nchunks_max = 0;
     int* err = nullptr;
     int64_t* scratch64 = nullptr;   // [2]: num-unique copy target, misc
@@ -461,7 +462,7 @@ int emb_create(const emb_table_spec* specs, int32_t num_tables, int32_t max_batc
          dalloc_n(L, &L->ukey_s, L->max_unique) && dalloc_n(L, &L->uslot_s, L->max_unique) &&
          dalloc_n(L, &L->bits_dev, 1) && dalloc_n(L, &L->slots, L->nchunks_max * 2 * kMaxDim) &&
          dalloc_n(L, &L->split_list, L->nchunks_max) && dalloc_n(L, &L->split_count, 4) &&
-         dalloc_n(L, &L->long_done, L->nchunks_max) &&
+         dalloc_n(L, &L->long_done, L->nchunks_max) && dalloc_n(L, &L->table_order, num_tables) &&
          dalloc_n(L, &L->err, 1) && dalloc_n(L, &L->scratch64, 2) && dalloc_n(L, &L->d_init_acc, num_tables);
     std::vector<int32_t> dyn;
     std::vector<float> init_acc(num_tables);
@@ -632,6 +633,7 @@ int emb_forward(emb_layer* L, const int64_t* keys, const int64_t* offsets, const
     a.bag_scale = L->bag_scale;
     a.sentinel = (uint32_t)L->total_rows;
     a.warps_per_table = (batch + 31) / 32;
+    a.order_buf = L->table_order;
     a.write_ids = true;
     a.rows16 = true;
     a.resolved = L->resolved;
@@ -977,6 +979,7 @@ int emb_forward_infer(emb_layer* L, const int64_t* keys, const int64_t* offsets,
     a.bag_scale = nullptr;
     a.sentinel = (uint32_t)L->total_rows;
     a.warps_per_table = (batch + 31) / 32;
+    a.order_buf = L->table_order;
     a.write_ids = false;
     a.rows16 = true;
     for (const TableDev& d : L->tabs) a.rows16 = a.rows16 && d.dtype != EMB_F32;

@@ -556,6 +556,22 @@ def main():
                 hout[b].copy_(dbuf[b]["out"], non_blocking=True)
                 ev_down[b].record(s_down)
 
+        # the host link's own rates on this machine, each way alone (best of 3
+        # copies of grad_out up and of the output down): what the copies of a
+        # step cost when nothing else runs
+        def link_gbs(dst, src):
+            best = float("inf")
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(comp)
+                dst.copy_(src, non_blocking=True)
+                e1.record(comp)
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1))
+            return src.numel() * src.element_size() / (best * 1e6)
+
+        h2d_gbs = link_gbs(dbuf[0]["g"], hg)
+        d2h_gbs = link_gbs(hout[0], dbuf[0]["out"])
         upload(0)
         for i in range(args.warmup):
             e2e_step(i)
@@ -577,7 +593,8 @@ def main():
         e2e = {"value": whole_job_rate(batches[0].nnz, ws, ems), "unit": "lookups/s", "ms_per_step": ems,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "copies": "pinned host <-> device, double-buffered on two copy streams overlapping compute; "
-                         "steady state: K uploads and K downloads inside the K timed steps"}
+                         "steady state: K uploads and K downloads inside the K timed steps",
+               "link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
     layer.close()
     if rank != 0:

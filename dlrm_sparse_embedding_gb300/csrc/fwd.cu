@@ -415,9 +415,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) fwd_pool(FwdArgs a)
                                                    out_col, bg0, ring);
 }
 
-// The tables in descending order of their lookups in this batch (ties by
+// The tables in descending order of their warps' expected duration (ties by
 // table index), for layers of at most kOrderThreads tables: one block; a
-// table's rank is the number of tables ahead of it.
+// table's rank is the number of tables ahead of it.  A lane group pools its
+// Lr bags one after another, a window of keys at a time, and a window costs
+// about the same whatever the row width, so a table's warps take about
+// (its lookups in this batch) x Lr.
 constexpr int kOrderThreads = 1024;
 
 __global__ void __launch_bounds__(kOrderThreads) fwd_order(FwdArgs a)
@@ -428,7 +431,9 @@ __global__ void __launch_bounds__(kOrderThreads) fwd_order(FwdArgs a)
         // clamped like the pooling kernel clamps them
         const int64_t lo = clamp_offset(__ldg(a.offsets + (int64_t)t * a.batch), 0, a.nnz);
         const int64_t hi = clamp_offset(__ldg(a.offsets + (int64_t)(t + 1) * a.batch), 0, a.nnz);
-        work[t] = hi > lo ? hi - lo : 0;
+        int lr = 1;
+        while (lr < ((a.tables[t].dim + 3) >> 2)) lr <<= 1;
+        work[t] = (hi > lo ? hi - lo : 0) * lr;
     }
     __syncthreads();
     for (int t = threadIdx.x; t < T; t += kOrderThreads) {
@@ -511,8 +516,8 @@ int launch_forward(const FwdArgs& args, cudaStream_t st)
                           : (a.rows16 ? fwd_pool<kBlocks16, false> : fwd_pool<3, false>);
     const int smem = ring_bytes(a.rows16 ? 8 : 16);
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -1;
-    // multi-hot batches (more lookups than bags): tables with the most lookups
-    // first, so the block scheduler does not end on a heavy table's blocks
+    // multi-hot batches (more lookups than bags): the tables with the longest
+    // warps first, so the block scheduler does not end on a heavy table's blocks
     a.order = nullptr;
     int launched = 1;
     if (a.order_buf && a.num_tables >= 2 && a.num_tables <= kOrderThreads &&

@@ -128,17 +128,33 @@ __device__ __forceinline__ int find_seg(const int32_t* p, int S, int64_t x)
 
 // The key a pass ranks: the input key, made local to its segment on the
 // first pass of the layer sort (all ones for a skipped or out-of-table id),
-// or with key_sub subtracted on the first pass of a plain sort.
+// or with key_sub subtracted on the first pass of a plain sort.  The
+// segment's table fields are read once per tile (FirstPass) and applied to
+// each of its keys.
+struct FirstPass {
+    uint32_t rb;      // the segment table's first global row
+    uint64_t rows;    // its rows
+    uint64_t sub;     // plain sort: subtracted from every key
+};
+
+__device__ __forceinline__ FirstPass first_pass_of(const SortArgs& a, int s, uint64_t sub)
+{
+    FirstPass f;
+    f.rb = a.tables ? a.tables[s].row_base : 0u;
+    f.rows = a.tables ? (uint64_t)a.tables[s].rows : 0ull;
+    f.sub = sub;
+    return f;
+}
+
 template <typename K>
-__device__ __forceinline__ K first_pass_key(const SortArgs& a, K k, int s, uint64_t sub)
+__device__ __forceinline__ K first_pass_key(const SortArgs& a, K k, const FirstPass& f)
 {
     if (a.tables) {
         const uint32_t g = (uint32_t)k;
-        const uint32_t rb = a.tables[s].row_base;
-        const uint64_t local = (uint64_t)g - rb;
-        return (g < a.sentinel && g >= rb && local < (uint64_t)a.tables[s].rows) ? (K)local : (K)a.skip_key;
+        const uint64_t local = (uint64_t)g - f.rb;
+        return (g < a.sentinel && g >= f.rb && local < f.rows) ? (K)local : (K)a.skip_key;
     }
-    return (K)(k - (K)sub);
+    return (K)(k - (K)f.sub);
 }
 
 // ---- segment and tile layout (one block) ----
@@ -308,6 +324,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_upsweep(SortArgs a, SortScr
                             : (c.dst_out ? static_cast<const K*>(a.keys_tmp) : static_cast<const K*>(a.keys_out));
     const int shift = pass * a.D;
     const uint64_t sub = (c.src_in && a.key_sub) ? *a.key_sub : 0ull;
+    const FirstPass fp = c.src_in ? first_pass_of(a, tl.s, sub) : FirstPass{0u, 0ull, 0ull};
     // all of the thread's keys are requested before the first is counted
     uint32_t dg[kSortItems];
 #pragma unroll
@@ -316,7 +333,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_upsweep(SortArgs a, SortScr
         dg[r] = (uint32_t)nb;
         if (e < tl.len) {
             K k = src[tl.start + e];
-            if (c.src_in) k = first_pass_key<K>(a, k, tl.s, sub);
+            if (c.src_in) k = first_pass_key<K>(a, k, fp);
             dg[r] = (uint32_t)((k >> shift) & (K)(nb - 1));
         }
     }
@@ -577,6 +594,7 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
         }
 
         for (int i = threadIdx.x; i < kWarps * nb / 2; i += kDownThreads) reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
+        const FirstPass fp = c.src_in ? first_pass_of(a, tl.s, sub) : FirstPass{0u, 0ull, 0ull};
         K k[kDownItems];
         uint32_t dg[kDownItems];
         uint32_t rk[kDownItems];
@@ -586,7 +604,7 @@ __global__ void __launch_bounds__(kDownThreads, kDownsweepBlocks) sort_downsweep
             k[r] = kr[r];
             dg[r] = (uint32_t)nb;
             if (e < tl.len) {
-                if (c.src_in) k[r] = first_pass_key<K>(a, k[r], tl.s, sub);
+                if (c.src_in) k[r] = first_pass_key<K>(a, k[r], fp);
                 dg[r] = (uint32_t)((k[r] >> shift) & (K)(nb - 1));
             }
         }

@@ -18,7 +18,9 @@
 // working precision rounded once; the result is stored into the bag's slice
 // of the concatenated output.  The same
 // pass writes, for the backward, the global row id (row_base + key) and the
-// bag of every lookup, and 1/L of every mean-pooled bag.
+// bag of every lookup, and 1/L of every mean-pooled bag.  For multi-hot
+// batches a small kernel first ranks the tables by their warps' expected
+// duration, and runs of warps take the tables longest first.
 #include <type_traits>
 
 #include "emb_internal.cuh"

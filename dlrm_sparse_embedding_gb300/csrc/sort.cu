@@ -22,7 +22,10 @@
 // and the number of significant key bits may live on the device (the
 // unique-based path only learns them there); passes beyond the significant
 // bits return at once, and the buffers are chosen so the last active pass
-// always writes the output.
+// always writes the output.  The histogram and ranking kernels are also
+// built with the digit count fixed (256 or 1024 digits), and the ranking
+// kernel with the pass's role fixed (first, middle, last, only) where the
+// host knows the number of passes.
 #include "emb_internal.cuh"
 
 namespace emb {
